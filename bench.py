@@ -1,0 +1,487 @@
+"""Benchmark of one paged decode step: KV write + decode attention (+ reduce).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config opt13b]
+                    [--impl ours|reference] [--partition P]
+
+A step is one pass of the hot path over one batch: the slot-mapped KV write
+of the step's new keys and values, then paged decode attention (partition
+pass and, when a sequence spans several partitions, the split-K merge); on
+the parallel-sampling workload the copy-on-write block copies run first.
+The default workload is the OPT-13B-shaped decode (40 heads MHA, head_dim
+128, fp16, block 16, batch 64, lengths uniform over 200..2000, shuffled pool
+= need + 10%), one layer.  Inputs are seeded synthetic data resident in HBM;
+the pool (about 1.6 GB) is larger than L2, so no flush is needed between
+steps.
+
+Under torchrun (N > 1) every rank runs its own batch on its own GPU with no
+collective on the data path (sequences are independent: weak scaling); the
+timed region is bracketed by barriers and the slowest rank's time is used.
+
+``--impl reference`` times the float64 CPU oracle on the same workload (one
+bounded sample of sequences per step) on rank 0; other ranks exit at once.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from paged_kv_cache_145_gb300 import synth  # noqa: E402
+
+METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
+
+# DRAM bytes (read + write) per launch of the decode kernels, from ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
+# hash of the kernel sources they were taken on.  A stale hash reports null.
+TRAFFIC = {}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in ("decode.cuh", "common.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_145_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            return float(json.load(fh)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# workload (product side: the native block manager plans the step)
+# ---------------------------------------------------------------------------
+class Workload:
+    def __init__(self, name, rank=0):
+        import paged_kv_cache_145_gb300 as pkv
+
+        cfg = synth.CONFIGS[name]
+        self.name, self.cfg = name, cfg
+        self.b = b = cfg["block_size"]
+        self.H, self.Hk, self.D, self.dtype = cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
+        self.elt = synth.ELEM_BYTES[self.dtype]
+        ceil_div = lambda a, c: -(-a // c)  # noqa: E731
+        if name == "fork":
+            g, f, prompt = cfg["groups"], cfg["forks"], cfg["prompt"]
+            self.ids = [i * f + j for i in range(g) for j in range(f)]
+            need = g * (ceil_div(prompt, b) + f - 1)
+        else:
+            lengths = synth.lengths(name)
+            self.ids = list(range(len(lengths)))
+            need = sum(ceil_div(int(t) + 1, b) for t in lengths)
+        self.N = cfg.get("pool_blocks") or synth.pool_with_slack(need, cfg["slack"])
+        bm = pkv.BlockManager(self.N, b, synth.free_order(synth.seed_of(name, 2) + rank, self.N))
+        if name == "fork":
+            for i in range(g):
+                bm.admit(i * f, prompt)
+                for j in range(1, f):
+                    bm.fork(i * f, i * f + j)
+        else:
+            for i, t in enumerate(lengths):
+                bm.admit(i, int(t))
+        self.slots, self.pairs = bm.append(self.ids)
+        self.max_blocks = max(bm.num_seq_blocks(i) for i in self.ids)
+        self.tables, self.seq_lens = bm.tables(self.ids, self.max_blocks)
+        self.S = len(self.ids)
+        self.max_len = int(self.seq_lens.max())
+
+    # Algorithmic bytes, counted without reuse across sequences.
+    def decode_bytes(self, part):
+        L = self.seq_lens.astype(np.int64)
+        kv = 2 * L * self.Hk * self.D * self.elt
+        qo = 2 * self.H * self.D * self.elt
+        table = 4 * (-(-L // self.b)) + 4
+        nparts = -(-L // part)
+        ws = np.where(nparts > 1, 2 * self.H * nparts * (self.D + 2) * 4, 0)
+        return int((kv + qo + table + ws).sum()), int(kv.sum())
+
+    def write_bytes(self):
+        n = self.S
+        return 2 * 2 * n * self.Hk * self.D * self.elt + 8 * n
+
+    def copy_bytes(self):
+        return 2 * 2 * len(self.pairs) * self.Hk * self.b * self.D * self.elt + 16 * len(self.pairs)
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def smi_gpu_id(local_index):
+    """nvidia-smi's name for a CUDA device: its UUID (robust to remapping)."""
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(local_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [x for x in vis.split(",") if x.strip()]
+        return ids[local_index] if local_index < len(ids) else str(local_index)
+
+
+class ClockSampler:
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.path = None
+        self.gpu = smi_gpu_id(gpu_index)
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + CLOCK_FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 9:
+                    continue
+                try:
+                    sm.append(float(f[1]))
+                    mx.append(float(f[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas; no data-path collective)
+# ---------------------------------------------------------------------------
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def combine_ranks(local_bytes, local_seconds):
+    """Whole-job throughput: bytes of all ranks over the slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+        b = torch.tensor([float(local_bytes)], dtype=torch.float64, device=dev)
+        s = torch.tensor([float(local_seconds)], dtype=torch.float64, device=dev)
+        dist.all_reduce(b, op=dist.ReduceOp.SUM)
+        dist.all_reduce(s, op=dist.ReduceOp.MAX)
+        return float(b.item()), float(s.item())
+    return float(local_bytes), float(local_seconds)
+
+
+def barrier():
+    import torch.distributed as dist
+
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle leg (spawned child, single BLAS thread)
+# ---------------------------------------------------------------------------
+def _oracle_sample(name, budget_s, max_seqs, seed):
+    """Times the oracle's KV write + attention over sequences of the workload
+    until ``budget_s`` seconds have passed; returns (kv_bytes, seconds, seqs)."""
+    from oracle import attention as A
+    from oracle import blocks as B
+    from oracle import paging as P
+
+    cfg = synth.CONFIGS[name]
+    b, H, Hk, D, dt = cfg["block_size"], cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
+    elt = synth.ELEM_BYTES[dt]
+    lengths = (synth.lengths(name) if name != "fork" else np.full(cfg["groups"] * cfg["forks"], cfg["prompt"]))
+    kv_bytes, done, spent = 0, 0, 0.0
+    for i, t in enumerate(lengths[:max_seqs]):
+        t = int(t)
+        nblk = P.blocks_needed(t + 1, b)
+        pool = B.BlockPool(nblk, b, free_order=synth.free_order(seed + i, nblk), auto_verify=False)
+        pool.admit(0, list(range(t)))
+        kp = synth.storage_numpy(synth.normal(seed + 3 * i, (nblk, Hk, b, D), dt), dt)
+        vp = synth.storage_numpy(synth.normal(seed + 3 * i + 1, (nblk, Hk, b, D), dt), dt)
+        kn = synth.storage_numpy(synth.normal(seed + 3 * i + 2, (1, Hk, D), dt), dt)
+        q = synth.storage_numpy(synth.normal(seed + 7 * i, (1, H, D), dt), dt)
+        t0 = time.perf_counter()
+        slot = pool.append(0, -1).slot
+        kp2, vp2, _ = A.write_tokens(kp, vp, kn, kn, [slot], b)
+        A.attention(q, kp2, vp2, [pool.table(0)], [t + 1], 1.0 / math.sqrt(D), b, dt)
+        spent += time.perf_counter() - t0
+        kv_bytes += 2 * (t + 1) * Hk * D * elt
+        done += 1
+        if spent >= budget_s:
+            break
+    return kv_bytes, spent, done
+
+
+def _oracle_child(conn, name, budget_s, max_seqs, seed):
+    conn.send(_oracle_sample(name, budget_s, max_seqs, seed))
+    conn.close()
+
+
+def oracle_timed(name, budget_s, max_seqs=10 ** 9, seed=4242):
+    """Runs the oracle sample in a spawned child limited to one BLAS thread."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    ctx = mp.get_context("spawn")
+    parent, child = ctx.Pipe()
+    p = ctx.Process(target=_oracle_child, args=(child, name, budget_s, max_seqs, seed))
+    p.start()
+    result = parent.recv()
+    p.join()
+    return result
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_timed(args.config, 0.0, max_seqs=1)
+    total_b, total_s, seqs = 0, 0.0, 0
+    for k in range(args.steps):
+        b, s, n = oracle_timed(args.config, 0.0, max_seqs=1, seed=4242 + 1000 * k)
+        total_b, total_s, seqs = total_b + b, total_s + s, seqs + n
+    gbs = total_b / total_s / 1e9
+    cfg = synth.CONFIGS[args.config]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 6), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * total_s / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.config, "about": cfg["about"],
+                   "sample": "one sequence of the workload per step, all heads"},
+        "decode_tokens_per_s": round(seqs / total_s, 3),
+        "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": "%d sequences, one per step, float64 NumPy oracle "
+                                   "(write + attention), 1 BLAS thread" % seqs},
+        "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import paged_kv_cache_145_gb300 as pkv
+
+    rank, local_rank, world = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    pkv._lib.lib()
+
+    # The CPU baseline child is spawned before any GPU work.
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_timed(args.config, args.cpu_budget)
+
+    w = Workload(args.config, rank=rank)
+    dt = synth.TORCH_DTYPE[w.dtype]
+    seed = synth.seed_of(args.config, 3) + 10 * rank
+    shape = (w.N, w.Hk, w.b, w.D)
+    cache = pkv.PagedKVCache(synth.normal(seed, shape, w.dtype, device="cuda"),
+                             synth.normal(seed + 1, shape, w.dtype, device="cuda"))
+    q_h = synth.normal(seed + 2, (w.S, w.H, w.D), w.dtype).pin_memory()
+    k_h = synth.normal(seed + 3, (w.S, w.Hk, w.D), w.dtype).pin_memory()
+    v_h = synth.normal(seed + 4, (w.S, w.Hk, w.D), w.dtype).pin_memory()
+    slots_h = torch.from_numpy(w.slots).pin_memory()
+    tables_h = torch.from_numpy(w.tables).pin_memory()
+    lens_h = torch.from_numpy(w.seq_lens).pin_memory()
+    pairs_h = torch.from_numpy(np.asarray(w.pairs, dtype=np.int64).reshape(-1, 2)).pin_memory()
+    q, k, v = q_h.to(dev), k_h.to(dev), v_h.to(dev)
+    slots, tables, lens, pairs = slots_h.to(dev), tables_h.to(dev), lens_h.to(dev), pairs_h.to(dev)
+    out = torch.empty_like(q)
+    out_h = torch.empty_like(q_h).pin_memory()
+    cref = pkv.PagedKVCache(cache.k_cache, cache.v_cache)
+    part = pkv.paged_attention_partition_size(cref, w.S, w.H, w.max_len, args.partition)
+    ws_bytes = pkv.paged_attention_workspace_bytes(cref, w.S, w.H, w.max_len, part)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+    scale = 1.0 / math.sqrt(w.D)
+    has_pairs = len(w.pairs) > 0
+    nparts_max = -(-w.max_len // part)
+    launches_per_step = 1 + 1 + (1 if nparts_max > 1 else 0) + (1 if has_pairs else 0)
+
+    stream = torch.cuda.current_stream()
+
+    def step(mid=None):
+        if has_pairs:
+            pkv.paged_block_copy(cache, pairs)
+        pkv.paged_kv_write(cache, k, v, slots)
+        if mid is not None:
+            mid.record(stream)
+        pkv.paged_attention_decode(cache, q, tables, lens, scale, out=out, max_seq_len=w.max_len,
+                                   workspace=ws, partition_size=part)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.paged_get_device_error() == 0
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    for i in range(args.steps):
+        starts[i].record(stream)
+        step(mids[i])
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    assert pkv.paged_get_device_error() == 0
+    total_ms = starts[0].elapsed_time(ends[-1])
+    decode_ms = statistics.fmean(mids[i].elapsed_time(ends[i]) for i in range(args.steps))
+
+    # End to end through the public API with host buffers: pinned host -> HBM
+    # copies of the step's inputs, the step, and the output back to the host.
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, k_h, v_h, slots_h, tables_h, lens_h))
+    if has_pairs:
+        h2d += pairs_h.numel() * pairs_h.element_size()
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_steps = args.steps
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        q.copy_(q_h, non_blocking=True)
+        k.copy_(k_h, non_blocking=True)
+        v.copy_(v_h, non_blocking=True)
+        slots.copy_(slots_h, non_blocking=True)
+        tables.copy_(tables_h, non_blocking=True)
+        lens.copy_(lens_h, non_blocking=True)
+        if has_pairs:
+            pairs.copy_(pairs_h, non_blocking=True)
+        step()
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+
+    dec_bytes, kv_bytes = w.decode_bytes(part)
+    step_bytes = dec_bytes + w.write_bytes() + (w.copy_bytes() if has_pairs else 0)
+    all_bytes, max_s = combine_ranks(step_bytes * args.steps, total_ms / 1e3)
+    all_e2e_bytes, max_e2e_s = combine_ranks(step_bytes * e2e_steps, e2e_ms / 1e3)
+    all_seqs, _ = combine_ranks(w.S * args.steps, total_ms / 1e3)
+    if rank != 0:
+        return
+    peak, peak_kind = hbm_peak()
+    achieved = dec_bytes / (decode_ms / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    tr = TRAFFIC.get(args.config)
+    traffic = tr[0] if tr and tr[1] == src_hash else None
+    line = {
+        "metric": METRIC,
+        "value": round(all_bytes / max_s / 1e9, 3),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(max_s * 1e3 / args.steps, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": args.config, "about": w.cfg["about"], "num_seqs": w.S,
+                   "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
+                   "pool_blocks": w.N, "partition_size": part,
+                   "l2": "no flush: the %.2f GB pool read per step exceeds the 129 MB L2"
+                         % (kv_bytes / 1e9),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "decode_tokens_per_s": round(all_seqs / max_s, 1),
+        "kv_gbs": round(kv_bytes / (decode_ms / 1e3) / 1e9, 3),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "paged_attention_decode (partition pass + split-K merge)",
+                     "peak_source": peak_kind, "decode_us": round(decode_ms * 1e3, 2),
+                     "decode_bytes": dec_bytes, "source_hash": src_hash},
+        "clocks": clocks,
+        "gpu_launches": launches_per_step * args.steps,
+        "e2e": {"value": round(all_e2e_bytes / max_e2e_s / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5)},
+    }
+    if cpu is not None:
+        cb, cs, cn = cpu
+        line["cpu_baseline"] = {
+            "value": round(cb / cs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d of %d sequences (all heads), KV write + attention, float64 NumPy "
+                      "oracle, 1 BLAS thread, %.1f s" % (cn, w.S, cs)}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--config", default="opt13b", choices=sorted(k for k in synth.CONFIGS if k != "tiny"))
+    ap.add_argument("--partition", type=int, default=0, help="positions per partition (0 = default)")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

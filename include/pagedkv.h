@@ -1,0 +1,272 @@
+/*
+ * pagedkv.h -- C ABI of a paged KV cache for single-query decode attention
+ * on NVIDIA GB300 (sm_103a).
+ *
+ * Sources (web pages, cited by title and section):
+ *   [vLLM-TGI] "Inside vLLM and TGI: Paging, Versioned Schedulers and
+ *              Operations": sections "Block addresses and fragmentation
+ *              arithmetic" and "Exact CPU block manager and copy-on-write".
+ *   [VM-LLM]   "vLLM and PagedAttention: Virtual Memory for LLM Serving"
+ *              (talk transcript, no headings: paragraphs on paging,
+ *              sharing / copy-on-write and preemption).
+ *   [CB-PA]    "Continuous Batching & PagedAttention: vLLM Memory
+ *              Management Architecture": "Core PagedAttention Mechanics".
+ *
+ * Model.  Keys and values of all sequences live in one shared pool of
+ * fixed-size physical blocks.  A sequence's block table lists, in logical
+ * order, the physical block holding each run of b positions: position t is
+ * in logical block t / b at offset t % b, and its physical block is
+ * table[t / b] ([vLLM-TGI] "Block addresses ..."; [CB-PA]).  The flat slot
+ * of a position is physical_block * b + offset.
+ *
+ * Cache layout (the pages leave it backend-specific; this library's choice):
+ * two arrays, k_cache and v_cache, each [num_blocks][num_kv_heads][b][D],
+ * row-major, element type pkv_cache.dtype.  One (block, KV head) page is a
+ * contiguous b * D run, which the kernels move with 16-byte aligned bulk
+ * copies.
+ *
+ * Ownership.  The caller owns every buffer.  All pointers in the GPU calls
+ * below are DEVICE pointers unless stated; the library keeps them only for
+ * the duration of the enqueued work and allocates no device memory.  Each
+ * call enqueues its kernels on `stream` and returns without synchronising.
+ * The only state the library keeps is one device error word per device
+ * (see paged_get_device_error) and the small per-device set-up it does on
+ * first use (kernel attributes, the error word's address).
+ *
+ * Errors.  Argument errors are found on the host, without synchronising:
+ * the call returns a negative PKV_ERR_* code and enqueues nothing.  Errors
+ * that depend on device-resident data (an out-of-range slot, table entry,
+ * length or block pair) are found by the kernels, which never trap: the
+ * offending item is skipped (attention rows are written as zeros) and a
+ * PKV_DEV_* bit is OR-ed into the device error word.  After a device error
+ * the caller should treat the pool as suspect.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Element type of q, the caches and out (one type for all of them). */
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+
+/* Host-side return codes. */
+#define PKV_OK              0
+#define PKV_ERR_NULL       -1  /* a required pointer is NULL                      */
+#define PKV_ERR_GEOMETRY   -2  /* unsupported block size, head dim or group size  */
+#define PKV_ERR_ARG        -3  /* bad count, length bound or partition size       */
+#define PKV_ERR_ALIGN      -4  /* a buffer is not 16-byte aligned                 */
+#define PKV_ERR_WORKSPACE  -5  /* workspace missing or too small                  */
+#define PKV_ERR_CUDA       -6  /* a CUDA runtime call or launch failed            */
+#define PKV_ERR_STATE      -7  /* block manager: unknown / duplicate sequence     */
+#define PKV_ERR_NOMEM      -8  /* block manager: not enough free blocks           */
+#define PKV_ERR_CAPACITY   -9  /* output table narrower than a sequence's table   */
+
+/* Device error bits (paged_get_device_error). */
+#define PKV_DEV_SLOT_RANGE   1u  /* paged_kv_write: slot >= num_blocks * b        */
+#define PKV_DEV_TABLE_RANGE  2u  /* decode: a used table entry not in [0, N)      */
+#define PKV_DEV_SEQ_LEN      4u  /* decode: length not in [1, max_seq_len]        */
+#define PKV_DEV_PAIR_RANGE   8u  /* paged_block_copy: src or dst not in [0, N)    */
+#define PKV_DEV_TIMEOUT     16u  /* a bounded wait for a bulk copy gave up        */
+
+/* The paged pool.  Supported geometry: block_size in {8, 16, 32},
+ * head_dim in {64, 128}.  k_cache / v_cache must be 16-byte aligned. */
+typedef struct {
+  void*   k_cache;       /* [num_blocks][num_kv_heads][block_size][head_dim] */
+  void*   v_cache;       /* same shape and type as k_cache                   */
+  int64_t num_blocks;    /* N: physical blocks in the pool                   */
+  int32_t block_size;    /* b: token positions per block                     */
+  int32_t num_kv_heads;  /* Hk                                               */
+  int32_t head_dim;      /* D                                                */
+  int32_t dtype;         /* a pkv_dtype                                      */
+} pkv_cache;
+
+/*
+ * paged_kv_write -- store each new token's key and value in its slot
+ * (the "reshape_and_cache" step).
+ *
+ * Follows [VM-LLM] (paging paragraph: tokens fill the last block, a new
+ * block is taken when it is full) and the append step of [vLLM-TGI]
+ * "Exact CPU block manager and copy-on-write".  For every i in
+ * [0, num_tokens) with slot = slot_mapping[i] >= 0:
+ *     k_cache[slot / b][h][slot % b][:] = k[i][h][:]   for every KV head h
+ *     v_cache[slot / b][h][slot % b][:] = v[i][h][:]
+ * Elements are copied bit for bit.  A negative slot marks padding and is
+ * skipped silently; a slot >= num_blocks * b is skipped and sets
+ * PKV_DEV_SLOT_RANGE.  Two tokens with the same slot race (last writer
+ * undefined).
+ *
+ *   k, v          device, [num_tokens][num_kv_heads][head_dim], contiguous,
+ *                 cache dtype, 16-byte aligned
+ *   slot_mapping  device, int64[num_tokens]
+ */
+int paged_kv_write(const pkv_cache* cache, const void* k, const void* v,
+                   const int64_t* slot_mapping, int64_t num_tokens,
+                   cudaStream_t stream);
+
+/*
+ * paged_attention_partition_size -- the partition length (in positions) a
+ * decode call will use.  `requested` = 0 selects the library default;
+ * otherwise it must be a positive multiple of block_size no larger than
+ * 8192 and is returned unchanged.  Returns a negative PKV_ERR_* on bad
+ * arguments.
+ */
+int32_t paged_attention_partition_size(const pkv_cache* cache, int32_t num_seqs,
+                                       int32_t num_heads, int32_t max_seq_len,
+                                       int32_t requested);
+
+/*
+ * paged_attention_workspace_bytes -- bytes of device workspace a decode
+ * call with these arguments needs (0 when every sequence fits in one
+ * partition).  Returns 0 and sets nothing on bad arguments; the decode
+ * call itself reports them.
+ *
+ * Workspace layout (float32, P = ceil(max_seq_len / partition_size)):
+ *   ml[num_seqs][num_heads][P]   as (m, l) float pairs: m = running maximum
+ *                                of the partition's scores in base-2 units
+ *                                (score * log2 e), l = sum of 2^(score - m)
+ *   o [num_seqs][num_heads][P][head_dim], starting at the next 256-byte
+ *                                boundary: the partition's normalised output
+ */
+size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
+                                       int32_t num_heads, int32_t max_seq_len,
+                                       int32_t partition_size);
+
+/*
+ * paged_attention_decode -- single-query attention of each sequence over
+ * its cached keys and values, read through its block table.
+ *
+ * The method: [vLLM-TGI] opening section and "Block addresses ..." (kernels
+ * read a sequence through its block table), [VM-LLM] paging paragraph (the
+ * attention kernel reads through the mapping; token order is unchanged).
+ * For sequence s, query head h and its KV head kh = h / (num_heads /
+ * num_kv_heads) (query heads grouped contiguously), with L = seq_lens[s]
+ * and K_t, V_t the rows of position t found through the table:
+ *     z_t = scale * dot(q[s][h], K_t)                    t = 0 .. L-1
+ *     out[s][h] = sum_t e^(z_t - max z) V_t / sum_t e^(z_t - max z)
+ * accumulated in float32 and rounded once to the output type.
+ *
+ * Long sequences are split into partitions of `partition_size` positions
+ * processed by separate thread blocks; a second kernel merges them
+ * (split-K).  Only the block-table entries covering positions < L are read.
+ *
+ *   q             device, [num_seqs][num_heads][head_dim], cache dtype
+ *   block_tables  device, int32[num_seqs][max_blocks_per_seq]
+ *   seq_lens      device, int32[num_seqs], positions to attend over
+ *   max_seq_len   host bound on seq_lens (0 = max_blocks_per_seq * b); it
+ *                 sizes the launch and the workspace
+ *   scale         multiplies every score (typically 1 / sqrt(head_dim))
+ *   out           device, [num_seqs][num_heads][head_dim], cache dtype
+ *   workspace     device, >= paged_attention_workspace_bytes(...) bytes,
+ *                 16-byte aligned; may be NULL when that is 0
+ *   partition_size 0 = default, else a multiple of block_size <= 8192
+ *
+ * num_heads must be num_kv_heads times 1, 2, 4 or 8.  A row whose length
+ * is outside [1, max_seq_len] (PKV_DEV_SEQ_LEN) or whose used table
+ * entries leave [0, num_blocks) (PKV_DEV_TABLE_RANGE) is written as zeros.
+ */
+int paged_attention_decode(const pkv_cache* cache, const void* q,
+                           const int32_t* block_tables, int32_t max_blocks_per_seq,
+                           const int32_t* seq_lens, int32_t num_seqs,
+                           int32_t num_heads, int32_t max_seq_len, float scale,
+                           void* out, void* workspace, size_t workspace_bytes,
+                           int32_t partition_size, cudaStream_t stream);
+
+/*
+ * paged_block_copy -- copy whole blocks, keys and values, every KV head:
+ *     block dst := block src   for each (src, dst) pair
+ *
+ * The copy half of copy-on-write: [vLLM-TGI] "Exact CPU block manager and
+ * copy-on-write" (appending to a shared, partially filled last block takes
+ * a fresh block and copies the old contents into it before the write) and
+ * [VM-LLM] sharing paragraph (a private copy for the branch being
+ * modified).  Enqueue it before the paged_kv_write that fills the new
+ * block.  Pairs with src or dst outside [0, num_blocks) are skipped and set
+ * PKV_DEV_PAIR_RANGE; src == dst is a no-op.  Destinations must be distinct
+ * and must not appear as a source in the same call (the copies run
+ * concurrently).
+ *
+ *   src_dst_pairs device, int64[num_pairs][2] as (src, dst)
+ */
+int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs,
+                     int64_t num_pairs, cudaStream_t stream);
+
+/*
+ * paged_get_device_error -- synchronise `stream`, then read and clear the
+ * current device's error word (an OR of PKV_DEV_* bits; 0 = no error).
+ * The word is shared by every stream on the device.
+ */
+int paged_get_device_error(cudaStream_t stream, uint32_t* bits);
+
+/* Text for a PKV_ERR_* code. */
+const char* paged_strerror(int code);
+
+/* ---------------------------------------------------------------------
+ * Host block manager: the allocator that decides block tables, slots and
+ * copy-on-write pairs (host memory only; no GPU calls).
+ *
+ * It follows [vLLM-TGI] "Exact CPU block manager and copy-on-write":
+ * admission takes ceil(len / b) blocks at once or fails with nothing
+ * taken; fork shares every block of the parent and counts one more
+ * reference; an append writes into the last block if it has room and is
+ * not shared, takes a fresh block when the last is full, and when the last
+ * is partial and shared takes a fresh block, records (old, fresh) for
+ * paged_block_copy, drops one reference from the old block and repoints the
+ * table; release drops one reference from every block and returns blocks
+ * that reach zero to the free list.  Free-list policy (left open by the
+ * pages): blocks are taken from the front of the list, the initial list is
+ * `free_order` (NULL = 0..N-1), and freed blocks go back to the front.
+ * Not thread-safe; sequences are named by caller-chosen int64 ids.
+ * ------------------------------------------------------------------- */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* free_order: host, int64[num_blocks], a permutation of 0..num_blocks-1, or
+ * NULL.  Returns NULL on bad arguments or host allocation failure. */
+pkv_block_manager* pkv_bm_create(int64_t num_blocks, int32_t block_size,
+                                 const int64_t* free_order);
+void pkv_bm_destroy(pkv_block_manager* bm);
+
+/* Admit sequence `seq` holding `num_tokens` (>= 1) positions. */
+int pkv_bm_admit(pkv_block_manager* bm, int64_t seq, int64_t num_tokens);
+
+/* Make `child` share every block of `parent`. */
+int pkv_bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child);
+
+/* One decode step: append one position to each of seqs[0..n-1], in order.
+ * Writes slot_mapping[i] (host, int64[n]) and the copy-on-write pairs the
+ * step needs (host, int64[n][2] capacity) with their count.  All or
+ * nothing: if the free list cannot cover every growth and copy of the step,
+ * returns PKV_ERR_NOMEM and changes nothing. */
+int pkv_bm_append(pkv_block_manager* bm, const int64_t* seqs, int64_t n,
+                  int64_t* slot_mapping, int64_t* pairs, int64_t* num_pairs);
+
+/* Drop the sequence and one reference from each of its blocks. */
+int pkv_bm_release(pkv_block_manager* bm, int64_t seq);
+
+/* Export tables (host, int32[n][max_blocks], padded with -1) and lengths
+ * (host, int32[n]) of seqs[0..n-1].  PKV_ERR_CAPACITY if a table is wider
+ * than max_blocks. */
+int pkv_bm_tables(const pkv_block_manager* bm, const int64_t* seqs, int64_t n,
+                  int32_t max_blocks, int32_t* tables, int32_t* seq_lens);
+
+int64_t pkv_bm_num_free(const pkv_block_manager* bm);
+int64_t pkv_bm_seq_len(const pkv_block_manager* bm, int64_t seq);     /* -1 if unknown */
+int64_t pkv_bm_num_seq_blocks(const pkv_block_manager* bm, int64_t seq); /* -1 if unknown */
+int32_t pkv_bm_refcount(const pkv_block_manager* bm, int64_t block);   /* -1 if out of range */
+
+/* Check the pool invariants: each count equals the table entries naming
+ * the block, the free list is duplicate-free and equals the blocks with
+ * count 0, every non-last block is full and the last holds 1..b positions.
+ * PKV_OK or PKV_ERR_STATE. */
+int pkv_bm_check(const pkv_block_manager* bm);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,237 @@
+"""GB300-native paged KV cache: decode attention, KV write and block copy.
+
+A thin binding over ``libpagedkv.so`` (C ABI: ``include/pagedkv.h``).  Each
+function checks and marshals its tensors (device, dtype, contiguity) and
+passes raw pointers and the CUDA stream to the library; every step of the
+computation runs in the library's CUDA kernels.  PyTorch supplies device
+memory and streams only.  There is no CPU fallback: if the library is not
+built, the first call raises.
+
+Cache layout: ``k_cache`` and ``v_cache`` are ``[num_blocks, kv_heads,
+block_size, head_dim]`` tensors of one dtype (float32, float16 or bfloat16).
+"""
+
+import ctypes
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import (PKV_DEV_PAIR_RANGE, PKV_DEV_SEQ_LEN, PKV_DEV_SLOT_RANGE,  # noqa: F401
+                   PKV_DEV_TABLE_RANGE, PKV_DEV_TIMEOUT, PKV_ERR_NOMEM)
+
+_DTYPE_CODE = {torch.float32: _lib.PKV_F32, torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16}
+
+__all__ = [
+    "PagedKVCache", "BlockManager", "paged_kv_write", "paged_attention_decode",
+    "paged_attention_workspace_bytes", "paged_attention_partition_size",
+    "paged_block_copy", "paged_get_device_error", "library_path",
+]
+
+
+def library_path():
+    return _lib.LIB_PATH
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must have dtype %s, got %s" % (name, dtype, t.dtype))
+    if device is not None and t.device != device:
+        raise ValueError("%s is on %s, the cache on %s" % (name, t.device, device))
+
+
+class PagedKVCache:
+    """The physical pool: two ``[N, Hk, b, D]`` tensors (keys, values)."""
+
+    def __init__(self, k_cache, v_cache):
+        _need(k_cache, "k_cache")
+        _need(v_cache, "v_cache", k_cache.dtype, k_cache.device)
+        if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+            raise ValueError("k_cache and v_cache must both be [N, Hk, b, D]")
+        if k_cache.dtype not in _DTYPE_CODE:
+            raise ValueError("cache dtype must be float32, float16 or bfloat16")
+        self.k_cache, self.v_cache = k_cache, v_cache
+        self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_cache.shape
+        self.dtype, self.device = k_cache.dtype, k_cache.device
+        self._c = _lib.pkv_cache(k_cache.data_ptr(), v_cache.data_ptr(), self.num_blocks,
+                                 self.block_size, self.num_kv_heads, self.head_dim,
+                                 _DTYPE_CODE[self.dtype])
+
+    @classmethod
+    def empty(cls, num_blocks, block_size, num_kv_heads, head_dim, dtype, device="cuda"):
+        shape = (num_blocks, num_kv_heads, block_size, head_dim)
+        return cls(torch.empty(shape, dtype=dtype, device=device),
+                   torch.empty(shape, dtype=dtype, device=device))
+
+    @property
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
+def paged_kv_write(cache, k, v, slot_mapping, stream=None):
+    """Store ``k``/``v`` ``[T, Hk, D]`` at ``slot_mapping`` (int64 ``[T]``)."""
+    _need(k, "k", cache.dtype, cache.device)
+    _need(v, "v", cache.dtype, cache.device)
+    _need(slot_mapping, "slot_mapping", torch.int64, cache.device)
+    n = slot_mapping.numel()
+    if k.shape != (n, cache.num_kv_heads, cache.head_dim) or v.shape != k.shape:
+        raise ValueError("k and v must be [num_tokens, kv_heads, head_dim]")
+    _lib.check(_lib.lib().paged_kv_write(cache.ref, _ptr(k), _ptr(v), _ptr(slot_mapping), n,
+                                         _stream(stream)), "paged_kv_write")
+
+
+def paged_attention_partition_size(cache, num_seqs, num_heads, max_seq_len, partition_size=0):
+    r = _lib.lib().paged_attention_partition_size(cache.ref, num_seqs, num_heads, max_seq_len,
+                                                  partition_size)
+    if r < 0:
+        _lib.check(r, "paged_attention_partition_size")
+    return r
+
+
+def paged_attention_workspace_bytes(cache, num_seqs, num_heads, max_seq_len, partition_size=0):
+    return int(_lib.lib().paged_attention_workspace_bytes(cache.ref, num_seqs, num_heads,
+                                                          max_seq_len, partition_size))
+
+
+def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, max_seq_len=0,
+                           workspace=None, partition_size=0, stream=None):
+    """Decode attention of ``q`` ``[S, H, D]`` through the block tables.
+
+    ``block_tables``: int32 ``[S, max_blocks]``; ``seq_lens``: int32 ``[S]``;
+    ``max_seq_len``: host bound on ``seq_lens`` (0 = table width x block
+    size).  Allocates ``out`` and the split-K workspace when not given.
+    Returns ``out``.
+    """
+    _need(q, "q", cache.dtype, cache.device)
+    _need(block_tables, "block_tables", torch.int32, cache.device)
+    _need(seq_lens, "seq_lens", torch.int32, cache.device)
+    if q.dim() != 3 or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads = q.shape[0], q.shape[1]
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or seq_lens.shape != (num_seqs,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", cache.dtype, cache.device)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    bound = max_seq_len if max_seq_len else block_tables.shape[1] * cache.block_size
+    need = paged_attention_workspace_bytes(cache, num_seqs, num_heads, bound, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=cache.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _lib.check(_lib.lib().paged_attention_decode(
+        cache.ref, _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
+        num_heads, max_seq_len, float(scale), _ptr(out), ws_ptr, ws_len, partition_size,
+        _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def paged_block_copy(cache, pairs, stream=None):
+    """Copy blocks ``pairs[i, 0] -> pairs[i, 1]`` (int64 ``[n, 2]``)."""
+    _need(pairs, "pairs", torch.int64, cache.device)
+    if pairs.numel() and (pairs.dim() != 2 or pairs.shape[1] != 2):
+        raise ValueError("pairs must be [num_pairs, 2]")
+    n = pairs.shape[0] if pairs.numel() else 0
+    _lib.check(_lib.lib().paged_block_copy(cache.ref, _ptr(pairs), n, _stream(stream)),
+               "paged_block_copy")
+
+
+def paged_get_device_error(stream=None):
+    """Synchronise the stream; return and clear the device error bits."""
+    bits = ctypes.c_uint32(0)
+    _lib.check(_lib.lib().paged_get_device_error(_stream(stream), ctypes.byref(bits)),
+               "paged_get_device_error")
+    return int(bits.value)
+
+
+def _i64(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int64))
+
+
+class BlockManager:
+    """Host block manager (native): tables, slots and copy-on-write pairs."""
+
+    def __init__(self, num_blocks, block_size, free_order=None):
+        self._lib = _lib.lib()
+        order = None
+        if free_order is not None:
+            order = _i64(free_order)
+            if order.shape != (num_blocks,):
+                raise ValueError("free_order must list every block once")
+        self._h = self._lib.pkv_bm_create(num_blocks, block_size,
+                                          None if order is None else order.ctypes.data)
+        if not self._h:
+            raise ValueError("bad block manager arguments")
+        self.num_blocks, self.block_size = num_blocks, block_size
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h:
+            self._lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def admit(self, seq, num_tokens):
+        rc = self._lib.pkv_bm_admit(self._h, seq, num_tokens)
+        if rc == PKV_ERR_NOMEM:
+            raise MemoryError("not enough free blocks to admit %d positions" % num_tokens)
+        _lib.check(rc, "admit")
+
+    def fork(self, parent, child):
+        _lib.check(self._lib.pkv_bm_fork(self._h, parent, child), "fork")
+
+    def append(self, seqs):
+        """Append one position to each sequence; returns (slots, pairs)."""
+        s = _i64(seqs)
+        n = s.shape[0]
+        slots = np.empty(n, dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+        npairs = ctypes.c_int64(0)
+        rc = self._lib.pkv_bm_append(self._h, s.ctypes.data, n, slots.ctypes.data,
+                                     pairs.ctypes.data, ctypes.byref(npairs))
+        if rc == PKV_ERR_NOMEM:
+            raise MemoryError("not enough free blocks for this step")
+        _lib.check(rc, "append")
+        return slots, pairs[: npairs.value].copy()
+
+    def release(self, seq):
+        _lib.check(self._lib.pkv_bm_release(self._h, seq), "release")
+
+    def tables(self, seqs, max_blocks):
+        s = _i64(seqs)
+        tab = np.empty((s.shape[0], max_blocks), dtype=np.int32)
+        lens = np.empty(s.shape[0], dtype=np.int32)
+        _lib.check(self._lib.pkv_bm_tables(self._h, s.ctypes.data, s.shape[0], max_blocks,
+                                           tab.ctypes.data, lens.ctypes.data), "tables")
+        return tab, lens
+
+    def num_free(self):
+        return int(self._lib.pkv_bm_num_free(self._h))
+
+    def seq_len(self, seq):
+        return int(self._lib.pkv_bm_seq_len(self._h, seq))
+
+    def num_seq_blocks(self, seq):
+        return int(self._lib.pkv_bm_num_seq_blocks(self._h, seq))
+
+    def refcount(self, block):
+        return int(self._lib.pkv_bm_refcount(self._h, block))
+
+    def check(self):
+        return self._lib.pkv_bm_check(self._h) == 0

@@ -1,0 +1,242 @@
+// C ABI entry points: host-side argument checks, dispatch, device error word.
+// The semantics of each call are documented in include/pagedkv.h.
+#include <cmath>
+#include <mutex>
+
+#include "decode.cuh"
+
+int pkv_launch_kv_write(const pkv_cache* c, const void* k, const void* v, const int64_t* slots,
+                        int64_t num_tokens, size_t elem_bytes, cudaStream_t stream);
+int pkv_launch_block_copy(const pkv_cache* c, const int64_t* pairs, int64_t num_pairs,
+                          size_t elem_bytes, cudaStream_t stream);
+int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
+int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
+int pkv_launch_decode_bf16(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
+
+// One error word per device, OR-ed by the kernels (PKV_DEV_* bits).
+static __device__ unsigned g_pkv_error;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_err_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+
+constexpr int kDefaultPartition = 512;
+
+size_t elem_bytes(int dtype) {
+  switch (dtype) {
+    case PKV_F32: return 4;
+    case PKV_F16: return 2;
+    case PKV_BF16: return 2;
+  }
+  return 0;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks common to every call that touches the pool.
+int check_cache(const pkv_cache* c) {
+  if (!c || !c->k_cache || !c->v_cache) return PKV_ERR_NULL;
+  if (elem_bytes(c->dtype) == 0) return PKV_ERR_ARG;
+  if (c->num_blocks < 1 || c->num_blocks > INT32_MAX || c->block_size < 1 ||
+      c->num_kv_heads < 1 || c->head_dim < 1)
+    return PKV_ERR_ARG;
+  if ((c->head_dim * elem_bytes(c->dtype)) % 16 != 0) return PKV_ERR_GEOMETRY;
+  if (!aligned16(c->k_cache) || !aligned16(c->v_cache)) return PKV_ERR_ALIGN;
+  return PKV_OK;
+}
+
+bool decode_geometry_ok(const pkv_cache* c, int num_heads) {
+  if (c->head_dim != 64 && c->head_dim != 128) return false;
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32) return false;
+  if (num_heads < 1 || num_heads % c->num_kv_heads) return false;
+  const int g = num_heads / c->num_kv_heads;
+  return g == 1 || g == 2 || g == 4 || g == 8;
+}
+
+int resolve_max_len(const pkv_cache* c, int32_t max_blocks, int32_t max_seq_len) {
+  const int64_t cap = (int64_t)max_blocks * c->block_size;
+  if (max_seq_len == 0) return cap > INT32_MAX ? -1 : (int)cap;
+  if (max_seq_len < 0 || max_seq_len > cap) return -1;
+  return max_seq_len;
+}
+
+int resolve_partition(const pkv_cache* c, int32_t requested) {
+  if (requested == 0) return kDefaultPartition;
+  if (requested < c->block_size || requested % c->block_size || requested > pkv::kMaxPartSize)
+    return PKV_ERR_ARG;
+  return requested;
+}
+
+struct WsLayout {
+  int parts;
+  size_t ml_bytes;
+  size_t o_offset;
+  size_t total;
+};
+
+WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_len, int part) {
+  WsLayout w{};
+  w.parts = (max_len + part - 1) / part;
+  if (w.parts <= 1) {
+    w.parts = 1;
+    return w;
+  }
+  const size_t rows = (size_t)num_seqs * num_heads * w.parts;
+  w.ml_bytes = rows * sizeof(float2);
+  w.o_offset = (w.ml_bytes + 255) & ~size_t(255);
+  w.total = w.o_offset + rows * head_dim * sizeof(float);
+  return w;
+}
+
+}  // namespace
+
+unsigned* pkv_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  if (!g_err_ptr[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pkv_error) != cudaSuccess) return nullptr;
+    g_err_ptr[dev] = static_cast<unsigned*>(ptr);
+  }
+  return g_err_ptr[dev];
+}
+
+extern "C" {
+
+int paged_kv_write(const pkv_cache* cache, const void* k, const void* v,
+                   const int64_t* slot_mapping, int64_t num_tokens, cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_tokens < 0 || num_tokens > INT32_MAX) return PKV_ERR_ARG;
+  if (num_tokens == 0) return PKV_OK;
+  if (!k || !v || !slot_mapping) return PKV_ERR_NULL;
+  if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PKV_ERR_ALIGN;
+  if (!pkv_error_word()) return PKV_ERR_CUDA;
+  return pkv_launch_kv_write(cache, k, v, slot_mapping, num_tokens, elem_bytes(cache->dtype),
+                             stream);
+}
+
+int32_t paged_attention_partition_size(const pkv_cache* cache, int32_t num_seqs,
+                                       int32_t num_heads, int32_t max_seq_len,
+                                       int32_t requested) {
+  if (!cache) return PKV_ERR_NULL;
+  if (num_seqs < 0 || num_heads < 1 || max_seq_len < 0) return PKV_ERR_ARG;
+  return resolve_partition(cache, requested);
+}
+
+size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
+                                       int32_t num_heads, int32_t max_seq_len,
+                                       int32_t partition_size) {
+  if (!cache || num_seqs < 1 || num_heads < 1 || max_seq_len < 1) return 0;
+  const int part = resolve_partition(cache, partition_size);
+  if (part < 0) return 0;
+  return workspace_layout(num_seqs, num_heads, cache->head_dim, max_seq_len, part).total;
+}
+
+int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                           int32_t num_heads, int32_t max_seq_len, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, int32_t partition_size,
+                           cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 1 || num_heads < 1)
+    return PKV_ERR_ARG;
+  if (num_seqs == 0) return PKV_OK;
+  if (!q || !out || !block_tables || !seq_lens) return PKV_ERR_NULL;
+  if (!decode_geometry_ok(cache, num_heads)) return PKV_ERR_GEOMETRY;
+  if (cache->num_kv_heads > 65535 || !std::isfinite(scale)) return PKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u))
+    return PKV_ERR_ALIGN;
+  const int max_len = resolve_max_len(cache, max_blocks_per_seq, max_seq_len);
+  if (max_len < 1) return PKV_ERR_ARG;
+  const int part = resolve_partition(cache, partition_size);
+  if (part < 0) return part;
+  const WsLayout ws = workspace_layout(num_seqs, num_heads, cache->head_dim, max_len, part);
+  if (ws.total > 0) {
+    if (!workspace) return PKV_ERR_WORKSPACE;
+    if (workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PKV_ERR_ALIGN;
+  }
+  unsigned* err = pkv_error_word();
+  if (!err) return PKV_ERR_CUDA;
+
+  pkv::DecodeParams p{};
+  p.k_cache = cache->k_cache;
+  p.v_cache = cache->v_cache;
+  p.num_blocks = cache->num_blocks;
+  p.kv_heads = cache->num_kv_heads;
+  p.num_heads = num_heads;
+  p.q = q;
+  p.out = out;
+  p.tables = block_tables;
+  p.max_blocks = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.max_len = max_len;
+  p.qscale = scale * 1.4426950408889634f;  // log2(e): scores in base-2 units
+  p.part_size = part;
+  p.num_parts = ws.parts;
+  p.ws_ml = ws.total ? static_cast<float2*>(workspace) : nullptr;
+  p.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_offset)
+                    : nullptr;
+  p.err = err;
+  const int group = num_heads / cache->num_kv_heads;
+  switch (cache->dtype) {
+    case PKV_F32:
+      return pkv_launch_decode_f32(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
+    case PKV_F16:
+      return pkv_launch_decode_f16(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
+    case PKV_BF16:
+      return pkv_launch_decode_bf16(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
+  }
+  return PKV_ERR_ARG;
+}
+
+int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs, int64_t num_pairs,
+                     cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_pairs < 0 || num_pairs > INT32_MAX) return PKV_ERR_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!src_dst_pairs) return PKV_ERR_NULL;
+  if (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u) return PKV_ERR_ALIGN;
+  if ((int64_t)cache->num_kv_heads * cache->block_size * cache->head_dim *
+          (int64_t)elem_bytes(cache->dtype) % 16)
+    return PKV_ERR_GEOMETRY;
+  if (!pkv_error_word()) return PKV_ERR_CUDA;
+  return pkv_launch_block_copy(cache, src_dst_pairs, num_pairs, elem_bytes(cache->dtype), stream);
+}
+
+int paged_get_device_error(cudaStream_t stream, uint32_t* bits) {
+  if (!bits) return PKV_ERR_NULL;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return PKV_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_pkv_error, sizeof(v)) != cudaSuccess) return PKV_ERR_CUDA;
+  const unsigned zero = 0;
+  if (cudaMemcpyToSymbol(g_pkv_error, &zero, sizeof(zero)) != cudaSuccess) return PKV_ERR_CUDA;
+  *bits = v;
+  return PKV_OK;
+}
+
+const char* paged_strerror(int code) {
+  switch (code) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_GEOMETRY: return "unsupported block size, head dim or head grouping";
+    case PKV_ERR_ARG: return "invalid count, length bound or partition size";
+    case PKV_ERR_ALIGN: return "buffer not aligned (16 bytes for data, element size for indices)";
+    case PKV_ERR_WORKSPACE: return "workspace missing or too small";
+    case PKV_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
+    case PKV_ERR_STATE: return "unknown or duplicate sequence id";
+    case PKV_ERR_NOMEM: return "not enough free blocks";
+    case PKV_ERR_CAPACITY: return "table wider than the output capacity";
+  }
+  return "unknown error code";
+}
+
+}  // extern "C"
