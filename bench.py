@@ -46,7 +46,10 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 # DRAM bytes (read + write) per launch of the decode kernels, from ncu
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on.  A stale hash reports null.
-TRAFFIC = {}
+TRAFFIC = {
+    "opt13b": (1280282888, "b57d4f0a238e7471"),
+    "gqa": (1124731408, "b57d4f0a238e7471"),
+}
 
 
 def kernel_source_hash():

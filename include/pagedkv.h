@@ -164,7 +164,9 @@ size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
  *   out           device, [num_seqs][num_heads][head_dim], cache dtype
  *   workspace     device, >= paged_attention_workspace_bytes(...) bytes,
  *                 16-byte aligned; may be NULL when that is 0
- *   partition_size 0 = default, else a multiple of block_size <= 8192
+ *   partition_size 0 = default, else a multiple of block_size <= 8192;
+ *                 at most 65535 partitions (max_seq_len / partition_size)
+ *   num_seqs      at most 65535
  *
  * num_heads must be num_kv_heads times 1, 2, 4 or 8.  A row whose length
  * is outside [1, max_seq_len] (PKV_DEV_SEQ_LEN) or whose used table

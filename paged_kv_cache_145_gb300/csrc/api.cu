@@ -158,6 +158,7 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
   const int part = resolve_partition(cache, partition_size);
   if (part < 0) return part;
   const WsLayout ws = workspace_layout(num_seqs, num_heads, cache->head_dim, max_len, part);
+  if (ws.parts > 65535) return PKV_ERR_ARG;  // partitions index the grid's z dimension
   if (ws.total > 0) {
     if (!workspace) return PKV_ERR_WORKSPACE;
     if (workspace_bytes < ws.total) return PKV_ERR_WORKSPACE;

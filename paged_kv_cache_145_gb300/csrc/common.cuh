@@ -96,6 +96,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+// 32-bit load through the non-coherent path, kept in program order with the
+// other loads written this way (so independent loads issue back to back).
+__device__ __forceinline__ int ld_nc(const int32_t* p) {
+  int v;
+  asm volatile("ld.global.nc.b32 %0, [%1];" : "=r"(v) : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ void set_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
 }

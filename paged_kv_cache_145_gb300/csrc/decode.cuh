@@ -16,7 +16,7 @@
 //   the G = H / Hk query heads that share the KV head, so each K/V page is
 //   read from HBM once for the whole group.
 //
-//   The partition is cut into chunks of C = min(b, 16) positions; chunk j
+//   The partition is cut into chunks of C = min(b, 8) positions; chunk j
 //   goes to warp j % 4.  Each warp owns a ring of kStages shared-memory
 //   stages; lane 0 fills a stage with two 1-D bulk copies (the chunk's keys
 //   and values for this head: C * D contiguous elements each, because the
@@ -79,16 +79,20 @@ constexpr int clog2(int x) { return x <= 1 ? 0 : 1 + clog2(x / 2); }
 
 template <typename T, int D, int BS, int G>
 struct DecodeCfg {
+  // Shape chosen by measurement on GB300: small rings (two 8-position stages
+  // per warp, 32 KiB per CTA) let up to 7 CTAs share an SM, and the extra
+  // resident warps hide each CTA's set-up latency; deeper rings with fewer
+  // CTAs per SM stream less.
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
-  static constexpr int kChunk = cmin(BS, 16);               // positions per stage
+  static constexpr int kChunk = cmin(BS, 8);                // positions per stage
   static constexpr int kChunksPerBlock = BS / kChunk;
   static constexpr int kLanesPerPos = 32 / kChunk;          // after the reduce-scatter
   static constexpr int kShift = clog2(kLanesPerPos);
   static constexpr int kDpl = D / 32;                       // elements per lane
   static constexpr int kChunkBytes = kChunk * D * (int)sizeof(T);
   static constexpr int kStageBytes = 2 * kChunkBytes;       // keys + values
-  static constexpr int kRingBudget = 96 * 1024;
+  static constexpr int kRingBudget = 32 * 1024;
   static constexpr int kStages = cmax(2, cmin(8, kRingBudget / (kWarps * kStageBytes)));
   static constexpr int kRingBytes = kWarps * kStages * kStageBytes;
   static constexpr int kBarOff = kRingBytes;
@@ -137,16 +141,29 @@ decode_partition_kernel(const DecodeParams p) {
   constexpr int SH = Cfg::kShift;
   extern __shared__ __align__(128) unsigned char smem[];
 
-  const int part = blockIdx.x;
-  const int kvh = blockIdx.y;
-  const int s = blockIdx.z;
+  // Partition is the slowest grid dimension: every sequence's first
+  // partition is dispatched before any second one, so the CTAs of partitions
+  // past a sequence's end (which exit at once) gather at the end of the grid.
+  const int kvh = blockIdx.x;
+  const int s = blockIdx.y;
+  const int part = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.num_heads;
   T* out = static_cast<T*>(p.out);
   const int64_t out0 = ((int64_t)s * H + (int64_t)kvh * G) * D;  // out[s][kvh*G][0]
+  const int PS = p.part_size;
+  const int tok0 = part * PS;
+  const int blk0 = tok0 / BS;
 
-  const int L = p.seq_lens[s];
+  // The length and this partition's table entries are loaded together (the
+  // entries speculatively, but never past the table row), so a CTA waits
+  // for one global round trip before it can issue its first bulk copy.
+  const int32_t* trow = p.tables + (int64_t)s * p.max_blocks + blk0;
+  const int span = min(PS / BS, p.max_blocks - blk0);
+  const int L = ld_nc(p.seq_lens + s);
+  const int e_first = (int)threadIdx.x < span ? ld_nc(trow + threadIdx.x) : -1;
+
   if (L < 1 || L > p.max_len) {
     if (part == 0) {
       for (int e = threadIdx.x; e < G * D; e += Cfg::kThreads) out[out0 + e] = Elem<T>::from_f(0.f);
@@ -154,12 +171,9 @@ decode_partition_kernel(const DecodeParams p) {
     }
     return;
   }
-  const int PS = p.part_size;
-  const int tok0 = part * PS;
   if (tok0 >= L) return;
   const int ntok = min(L - tok0, PS);
   const int nparts = (L + PS - 1) / PS;
-  const int blk0 = tok0 / BS;
   const int nblk = (ntok + BS - 1) / BS;
   const int nchunks = (ntok + C - 1) / C;
 
@@ -173,8 +187,11 @@ decode_partition_kernel(const DecodeParams p) {
     fence_mbar_init();
   }
   int bad = 0;
-  const int32_t* trow = p.tables + (int64_t)s * p.max_blocks + blk0;
-  for (int i = threadIdx.x; i < nblk; i += Cfg::kThreads) {
+  if ((int)threadIdx.x < nblk) {
+    bad = (e_first < 0 || (int64_t)e_first >= p.num_blocks);
+    stable[threadIdx.x] = e_first;
+  }
+  for (int i = threadIdx.x + Cfg::kThreads; i < nblk; i += Cfg::kThreads) {
     const int e = trow[i];
     bad |= (e < 0 || (int64_t)e >= p.num_blocks);
     stable[i] = e;
@@ -190,18 +207,6 @@ decode_partition_kernel(const DecodeParams p) {
       p.ws_ml[ws0 + (int64_t)threadIdx.x * p.num_parts] = make_float2(-INFINITY, -1.f);
     }
     return;
-  }
-
-  // Query rows of the group, pre-scaled into base-2 score units.
-  float qv[G][DPL];
-  {
-    const T* qp = static_cast<const T*>(p.q) + out0 + lane * DPL;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      RowLoad<T, DPL>::load(qp + g * D, qv[g]);
-#pragma unroll
-      for (int d = 0; d < DPL; ++d) qv[g][d] *= p.qscale;
-    }
   }
 
   const int count = warp < nchunks ? (nchunks - warp + NW - 1) / NW : 0;
@@ -226,6 +231,19 @@ decode_partition_kernel(const DecodeParams p) {
   if (lane == 0) {
     const int pre = count < NST ? count : NST;
     for (int j = 0; j < pre; ++j) issue(j);
+  }
+
+  // Query rows of the group, pre-scaled into base-2 score units (loaded while
+  // the first copies are in flight).
+  float qv[G][DPL];
+  {
+    const T* qp = static_cast<const T*>(p.q) + out0 + lane * DPL;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      RowLoad<T, DPL>::load(qp + g * D, qv[g]);
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) qv[g][d] *= p.qscale;
+    }
   }
 
   float m[G], l[G], acc[G][DPL];
@@ -437,7 +455,25 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
   for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
   float tot = 0.f;
   const float* o = p.ws_o + row * D + lane * DPL;
-  for (int i = 0; i < nparts; ++i) {
+  // Four partitions per round, loads first, so their latencies overlap.
+  int i = 0;
+  for (; i + 4 <= nparts; i += 4) {
+    float2 v[4];
+    float of[4][DPL];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      v[u] = ml[i + u];
+      RowLoad<float, DPL>::load(o + (int64_t)(i + u) * D, of[u]);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float w = v[u].y * exp2f(v[u].x - big);
+      tot += w;
+#pragma unroll
+      for (int d = 0; d < DPL; ++d) acc[d] = fmaf(w, of[u][d], acc[d]);
+    }
+  }
+  for (; i < nparts; ++i) {
     const float2 v = ml[i];
     const float w = v.y * exp2f(v.x - big);
     tot += w;
@@ -468,7 +504,7 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, cudaStream_t stream) 
       return PKV_ERR_CUDA;
     ready.fetch_or(bit);
   }
-  dim3 grid((unsigned)p.num_parts, (unsigned)p.kv_heads, (unsigned)num_seqs);
+  dim3 grid((unsigned)p.kv_heads, (unsigned)num_seqs, (unsigned)p.num_parts);
   kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
   if (p.num_parts > 1) {
     dim3 g2((unsigned)((p.num_heads + 3) / 4), (unsigned)num_seqs);

@@ -1,0 +1,59 @@
+"""Host-side logic of bench.py (no GPU): byte accounting pinned to the pages'
+per-token KV figure, and the rank-combining rule run on 2 gloo ranks."""
+
+import os
+import socket
+
+import numpy as np
+import torch.multiprocessing as tmp
+
+import bench
+from oracle import paging as P
+
+
+def test_decode_bytes_per_position_match_kv_sizing():
+    # OPT-13B: about 800 KB of KV per token over 40 layers ("vLLM and
+    # PagedAttention: Virtual Memory for LLM Serving", sizing paragraph), so
+    # one layer's keys + values are 1/40 of the oracle's per-token figure.
+    w = bench.Workload("opt13b")
+    _, kv = w.decode_bytes(512)
+    per_pos = kv / int(w.seq_lens.sum())
+    assert per_pos == P.kv_bytes_per_token(40, 5120, 2) / 40 == 20480
+    g = bench.Workload("gqa")
+    _, kv = g.decode_bytes(512)
+    assert kv / int(g.seq_lens.sum()) == 2 * 8 * 128 * 2
+
+
+def test_workload_plans_one_new_position_per_sequence():
+    w = bench.Workload("opt13b")
+    assert len(w.slots) == w.S == 64 and len(w.pairs) == 0
+    assert np.all(w.seq_lens == bench.synth.lengths("opt13b") + 1)
+    f = bench.Workload("fork")
+    assert len(f.pairs) == 16 * 7
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, results):
+    import torch.distributed as dist
+
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    b, s = bench.combine_ranks(1000 * (rank + 1), 0.5 + rank)
+    results[rank] = (b, s)
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_combine_ranks_two_gloo_ranks():
+    port = _free_port()
+    mgr = tmp.Manager()
+    results = mgr.dict()
+    tmp.spawn(_rank, args=(2, port, results), nprocs=2, join=True)
+    assert results[0] == results[1] == (3000.0, 1.5)
