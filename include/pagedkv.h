@@ -180,6 +180,39 @@ int paged_attention_decode(const pkv_cache* cache, const void* q,
                            int32_t partition_size, cudaStream_t stream);
 
 /*
+ * paged_attention_decode_static_ws -- paged_attention_decode without a
+ * caller-supplied workspace.  The pages have no counterpart to this call; it
+ * exists for callers that cannot allocate device memory themselves (a
+ * plug-in inside a host program that owns and reserves GPU memory up front,
+ * a latency-critical path where cudaMalloc may synchronise the device, a
+ * plain C caller without a caching allocator).
+ *
+ * Same arguments, semantics and errors as paged_attention_decode, minus
+ * `workspace` and `workspace_bytes`: the split-K scratch is one fixed device
+ * array of PKV_STATIC_WS_BYTES bytes inside the library, held by every
+ * device that loads it until the process exits.  The call allocates nothing
+ * (no cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ *   - A request whose scratch, as paged_attention_workspace_bytes would
+ *     report it, exceeds PKV_STATIC_WS_BYTES returns PKV_ERR_WORKSPACE and
+ *     enqueues nothing.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and caches it; make
+ *     that first call before any stream capture.
+ *   - All calls share the one array.  Calls whose kernels overlap on the GPU
+ *     (different streams, no ordering between them) race on it and give
+ *     wrong results; order them on one stream or with events.  Each call
+ *     writes every scratch entry it reads, so nothing carries over between
+ *     calls and nothing needs clearing.
+ */
+#define PKV_STATIC_WS_BYTES (32u << 20)
+int paged_attention_decode_static_ws(const pkv_cache* cache, const void* q,
+                                     const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                     const int32_t* seq_lens, int32_t num_seqs,
+                                     int32_t num_heads, int32_t max_seq_len, float scale,
+                                     void* out, int32_t partition_size, cudaStream_t stream);
+
+/*
  * paged_block_copy -- copy whole blocks, keys and values, every KV head:
  *     block dst := block src   for each (src, dst) pair
  *

@@ -18,7 +18,9 @@ PKV_DEV_SEQ_LEN = 4
 PKV_DEV_PAIR_RANGE = 8
 PKV_DEV_TIMEOUT = 16
 
+PKV_ERR_WORKSPACE = -5
 PKV_ERR_NOMEM = -8
+PKV_STATIC_WS_BYTES = 32 << 20
 
 
 class pkv_cache(ctypes.Structure):
@@ -45,6 +47,8 @@ SIGNATURES = {
     "paged_attention_workspace_bytes": (ctypes.c_size_t, [_CACHE, _I32, _I32, _I32, _I32]),
     "paged_attention_decode": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
                                               ctypes.c_float, _P, _P, ctypes.c_size_t, _I32, _P]),
+    "paged_attention_decode_static_ws": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
+                                                        ctypes.c_float, _P, _I32, _P]),
     "paged_block_copy": (ctypes.c_int, [_CACHE, _P, _I64, _P]),
     "paged_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "paged_strerror": (ctypes.c_char_p, [ctypes.c_int]),
