@@ -1,17 +1,24 @@
 // C ABI entry points: host-side argument checks, dispatch, device error word.
 // The semantics of each call are documented in include/pagedkv.h.
+#include <cudaTypedefs.h>
+
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
-#include "decode.cuh"
+#include "decode_launch.cuh"
 
 int pkv_launch_kv_write(const pkv_cache* c, const void* k, const void* v, const int64_t* slots,
                         int64_t num_tokens, size_t elem_bytes, cudaStream_t stream);
 int pkv_launch_block_copy(const pkv_cache* c, const int64_t* pairs, int64_t num_pairs,
                           size_t elem_bytes, cudaStream_t stream);
-int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
-int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
-int pkv_launch_decode_bf16(const pkv::DecodeParams&, int, int, int, int, cudaStream_t);
+int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
+                          cudaStream_t);
+int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
+                          cudaStream_t);
+int pkv_launch_decode_bf16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
+                           cudaStream_t);
 
 // One error word per device, OR-ed by the kernels (PKV_DEV_* bits).
 static __device__ unsigned g_pkv_error;
@@ -88,6 +95,48 @@ WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_len
   w.o_offset = (w.ml_bytes + 255) & ~size_t(255);
   w.total = w.o_offset + rows * head_dim * sizeof(float);
   return w;
+}
+
+// The tensor-core decode kernel serves fp16 / bf16 pools whose query heads
+// come in groups of 2, 4 or 8 and whose blocks hold a multiple of 16
+// positions.  PKV_DECODE_KERNEL=simt in the environment selects the
+// CUDA-core kernel instead (read on every call).
+bool use_mma(const pkv_cache* c, int group) {
+  if (c->dtype == PKV_F32 || group < 2 || c->block_size % 16) return false;
+  const char* env = std::getenv("PKV_DECODE_KERNEL");
+  return !(env && std::strcmp(env, "simt") == 0);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Describes a [N][Hk][b][D] pool as a 4-D tensor (D fastest) read in boxes of
+// 16 rows x 64 elements (128 bytes) with the 128-byte shared-memory swizzle.
+bool encode_pool_map(CUtensorMap* map, const pkv_cache* c, void* base) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t elt = elem_bytes(c->dtype);
+  const cuuint64_t dims[4] = {(cuuint64_t)c->head_dim, (cuuint64_t)c->block_size,
+                              (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->num_blocks};
+  const cuuint64_t strides[3] = {c->head_dim * elt, c->block_size * c->head_dim * elt,
+                                 (cuuint64_t)c->num_kv_heads * c->block_size * c->head_dim * elt};
+  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty =
+      c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  return enc(map, ty, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -187,13 +236,19 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
                     : nullptr;
   p.err = err;
   const int group = num_heads / cache->num_kv_heads;
+  pkv::DecodeMaps maps;
+  const pkv::DecodeMaps* mp = nullptr;
+  if (use_mma(cache, group)) {
+    if (!encode_pool_map(&maps.k, cache, cache->k_cache) ||
+        !encode_pool_map(&maps.v, cache, cache->v_cache))
+      return PKV_ERR_CUDA;
+    mp = &maps;
+  }
+  const int D = cache->head_dim, B = cache->block_size;
   switch (cache->dtype) {
-    case PKV_F32:
-      return pkv_launch_decode_f32(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
-    case PKV_F16:
-      return pkv_launch_decode_f16(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
-    case PKV_BF16:
-      return pkv_launch_decode_bf16(p, num_seqs, cache->head_dim, cache->block_size, group, stream);
+    case PKV_F32: return pkv_launch_decode_f32(p, num_seqs, D, B, group, mp, stream);
+    case PKV_F16: return pkv_launch_decode_f16(p, num_seqs, D, B, group, mp, stream);
+    case PKV_BF16: return pkv_launch_decode_bf16(p, num_seqs, D, B, group, mp, stream);
   }
   return PKV_ERR_ARG;
 }

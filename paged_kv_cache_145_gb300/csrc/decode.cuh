@@ -486,63 +486,4 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
   for (int d = 0; d < DPL; ++d) out[d] = Elem<T>::from_f(acc[d] / tot);
 }
 
-// ---------------------------------------------------------------------------
-// Host launchers
-// ---------------------------------------------------------------------------
-template <typename T, int D, int BS, int G>
-int launch_decode_cfg(const DecodeParams& p, int num_seqs, cudaStream_t stream) {
-  using Cfg = DecodeCfg<T, D, BS, G>;
-  auto kern = decode_partition_kernel<T, D, BS, G>;
-  // Opt in to more than 48 KB of dynamic shared memory, once per device.
-  static std::atomic<uint64_t> ready{0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
-  const uint64_t bit = 1ull << (dev & 63);
-  if (!(ready.load() & bit)) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kMaxSmem) !=
-        cudaSuccess)
-      return PKV_ERR_CUDA;
-    ready.fetch_or(bit);
-  }
-  dim3 grid((unsigned)p.kv_heads, (unsigned)num_seqs, (unsigned)p.num_parts);
-  kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
-  if (p.num_parts > 1) {
-    dim3 g2((unsigned)((p.num_heads + 3) / 4), (unsigned)num_seqs);
-    decode_reduce_kernel<T, D><<<g2, 128, 0, stream>>>(p);
-  }
-  return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
-}
-
-template <typename T, int D, int BS>
-int launch_decode_g(const DecodeParams& p, int num_seqs, int group, cudaStream_t stream) {
-  switch (group) {
-    case 1: return launch_decode_cfg<T, D, BS, 1>(p, num_seqs, stream);
-    case 2: return launch_decode_cfg<T, D, BS, 2>(p, num_seqs, stream);
-    case 4: return launch_decode_cfg<T, D, BS, 4>(p, num_seqs, stream);
-    case 8: return launch_decode_cfg<T, D, BS, 8>(p, num_seqs, stream);
-  }
-  return PKV_ERR_GEOMETRY;
-}
-
-template <typename T, int D>
-int launch_decode_b(const DecodeParams& p, int num_seqs, int block_size, int group,
-                    cudaStream_t stream) {
-  switch (block_size) {
-    case 8: return launch_decode_g<T, D, 8>(p, num_seqs, group, stream);
-    case 16: return launch_decode_g<T, D, 16>(p, num_seqs, group, stream);
-    case 32: return launch_decode_g<T, D, 32>(p, num_seqs, group, stream);
-  }
-  return PKV_ERR_GEOMETRY;
-}
-
-template <typename T>
-int launch_decode(const DecodeParams& p, int num_seqs, int head_dim, int block_size, int group,
-                  cudaStream_t stream) {
-  switch (head_dim) {
-    case 64: return launch_decode_b<T, 64>(p, num_seqs, block_size, group, stream);
-    case 128: return launch_decode_b<T, 128>(p, num_seqs, block_size, group, stream);
-  }
-  return PKV_ERR_GEOMETRY;
-}
-
 }  // namespace pkv

@@ -1,8 +1,8 @@
 // Decode attention instantiations for one cache element type (split per type
 // so the three translation units compile in parallel).
-#include "decode.cuh"
+#include "decode_launch.cuh"
 
 int pkv_launch_decode_bf16(const pkv::DecodeParams& p, int num_seqs, int head_dim, int block_size,
-                        int group, cudaStream_t stream) {
-  return pkv::launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, block_size, group, stream);
+                        int group, const pkv::DecodeMaps* maps, cudaStream_t stream) {
+  return pkv::launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, block_size, group, maps, stream);
 }

@@ -69,8 +69,19 @@ GRID += [("f16", 128, 16, 2, 0), ("f16", 128, 16, 8, 0), ("bf16", 128, 16, 8, 2)
          ("bf16", 64, 8, 2, 2), ("f32", 128, 32, 8, 0)]
 
 
+@pytest.fixture(params=["auto", "simt"])
+def kernel(request, monkeypatch):
+    """Runs a test with the automatic kernel choice (tensor cores for grouped
+    fp16/bf16 heads) and again with the CUDA-core kernel forced."""
+    if request.param == "simt":
+        monkeypatch.setenv("PKV_DECODE_KERNEL", "simt")
+    else:
+        monkeypatch.delenv("PKV_DECODE_KERNEL", raising=False)
+    return request.param
+
+
 @pytest.mark.parametrize("dt,D,b,G,part", GRID)
-def test_geometry_grid(dt, D, b, G, part):
+def test_geometry_grid(dt, D, b, G, part, kernel):
     # part = 2 means two blocks per partition: many partitions, ragged tails.
     lens = [1, b - 1, b, b + 1, 97, 300, 2 * b * 3 + 5]
     c = Case(dt, 2 * G, 2, D, b, lens, seed=hash((dt, D, b, G, part)) % 1000)
@@ -108,7 +119,7 @@ def test_equal_keys_give_mean_of_values(part):
 
 
 @pytest.mark.parametrize("part", [0, 64])
-def test_partition_boundaries(part):
+def test_partition_boundaries(part, kernel):
     lens = [63, 64, 65, 127, 128, 129, 511, 512, 513, 1023, 1024, 1025]
     c = Case("bf16", 8, 2, 128, 16, lens, seed=5)
     out, err = c.gpu(part=part)
@@ -133,7 +144,7 @@ def test_invalid_lengths_zero_rows():
 
 
 @pytest.mark.parametrize("part", [0, 32])
-def test_bad_table_entry_zero_row(part):
+def test_bad_table_entry_zero_row(part, kernel):
     c = Case("bf16", 8, 2, 128, 16, [100, 100, 100], seed=7)
     tables = c.tables.copy()
     tables[1, 3] = c.N + 7
@@ -158,7 +169,7 @@ def test_unused_table_entries_are_not_read():
 
 
 @pytest.mark.parametrize("part", [0, 48])
-def test_relabelling_blocks_is_bit_exact(part):
+def test_relabelling_blocks_is_bit_exact(part, kernel):
     c = Case("bf16", 16, 4, 128, 16, [200, 17, 700, 1], seed=9)
     out1, _ = c.gpu(part=part)
     perm = torch.from_numpy(np.random.default_rng(1).permutation(c.N))
@@ -175,7 +186,7 @@ def test_relabelling_blocks_is_bit_exact(part):
     assert torch.equal(out1, out2)
 
 
-def test_shared_prefix_forks_identical():
+def test_shared_prefix_forks_identical(kernel):
     c = Case("bf16", 32, 8, 128, 16, [1031] * 4, seed=10)
     tables = np.repeat(c.tables[:1], 4, axis=0)
     q = c.q.clone()
@@ -223,3 +234,21 @@ def test_empty_batch_is_a_no_op():
     out = pkv.paged_attention_decode(cache, q, torch.empty(0, 1, dtype=torch.int32, device="cuda"),
                                      torch.empty(0, dtype=torch.int32, device="cuda"), 0.1)
     assert out.shape == (0, 4, 64) and pkv.paged_get_device_error() == 0
+
+
+@pytest.mark.parametrize("dt,G", [("bf16", 4), ("f16", 8), ("f16", 1), ("f32", 4)])
+def test_stale_nan_slots_never_reach_the_output(dt, G, kernel):
+    # Slots past each sequence's end inside its last block hold NaN; the
+    # kernels must neither use them nor let 0 * NaN into the sums.
+    lens = [1, 5, 16, 17, 31, 250]
+    c = Case(dt, 2 * G, 2, 128, 16, lens, seed=13)
+    for s_, L in enumerate(lens):
+        last = int(c.tables[s_, (L - 1) // 16])
+        c.k[last, :, (L - 1) % 16 + 1:] = float("nan")
+        c.v[last, :, (L - 1) % 16 + 1:] = float("nan")
+    out, err = c.gpu(part=32)
+    assert err == 0
+    got = gpu_out_f64(out)
+    ref, _ = c.oracle()
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= edge_tol(dt, ref))
