@@ -419,24 +419,35 @@ decode_partition_kernel(const DecodeParams p) {
 }
 
 // Merges the partitions of every (sequence, query head) whose sequence needed
-// more than one: one warp per head, 4 heads per CTA.
-template <typename T, int D>
-__global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p) {
+// more than one.  A CTA of 4 warps covers 4 / WPH heads of one sequence with
+// WPH warps per head: every warp reads all (m, l) pairs of its head to find
+// the common maximum M (they are few), then the head's warps accumulate its
+// partitions round-robin with loads issued four at a time and their partial
+// sums meet in shared memory.  WPH = 1 suits a handful of partitions, WPH = 4
+// long contexts with dozens.
+constexpr int kReduceWarps = 4;
+
+template <typename T, int D, int WPH>
+__global__ void __launch_bounds__(kReduceWarps * 32) decode_reduce_kernel(const DecodeParams p) {
   constexpr int DPL = D / 32;
+  constexpr int NW = kReduceWarps;
+  __shared__ float part_acc[NW][D];
+  __shared__ float part_tot[NW];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int sub = warp % WPH;
+  const int h = blockIdx.x * (NW / WPH) + warp / WPH;
   const int s = blockIdx.y;
-  const int h = blockIdx.x * 4 + warp;
-  if (h >= p.num_heads) return;
   const int L = p.seq_lens[s];
   if (L < 1 || L > p.max_len) return;  // the partition pass wrote zeros
   const int nparts = (L + p.part_size - 1) / p.part_size;
   if (nparts <= 1) return;  // the partition pass wrote the output
-  const int64_t row = ((int64_t)s * p.num_heads + h) * p.num_parts;
+  const bool live = h < p.num_heads;
+  const int64_t row = ((int64_t)s * p.num_heads + (live ? h : 0)) * p.num_parts;
   const float2* ml = p.ws_ml + row;
   float big = -INFINITY;
   bool bad = false;
-  for (int i = lane; i < nparts; i += 32) {
+  for (int i = lane; live && i < nparts; i += 32) {
     const float2 v = ml[i];
     bad |= v.y < 0.f;
     big = fmaxf(big, v.x);
@@ -444,26 +455,19 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
 #pragma unroll
   for (int off = 16; off >= 1; off >>= 1) big = fmaxf(big, __shfl_xor_sync(kFullMask, big, off));
   bad = __any_sync(kFullMask, bad);
-  T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + h) * D + lane * DPL;
-  if (bad) {
-#pragma unroll
-    for (int d = 0; d < DPL; ++d) out[d] = Elem<T>::from_f(0.f);
-    return;
-  }
   float acc[DPL];
 #pragma unroll
   for (int d = 0; d < DPL; ++d) acc[d] = 0.f;
   float tot = 0.f;
   const float* o = p.ws_o + row * D + lane * DPL;
-  // Four partitions per round, loads first, so their latencies overlap.
-  int i = 0;
-  for (; i + 4 <= nparts; i += 4) {
+  int i = sub;
+  for (; live && !bad && i + 3 * WPH < nparts; i += 4 * WPH) {
     float2 v[4];
     float of[4][DPL];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      v[u] = ml[i + u];
-      RowLoad<float, DPL>::load(o + (int64_t)(i + u) * D, of[u]);
+      v[u] = ml[i + u * WPH];
+      RowLoad<float, DPL>::load(o + (int64_t)(i + u * WPH) * D, of[u]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -473,7 +477,7 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
       for (int d = 0; d < DPL; ++d) acc[d] = fmaf(w, of[u][d], acc[d]);
     }
   }
-  for (; i < nparts; ++i) {
+  for (; live && !bad && i < nparts; i += WPH) {
     const float2 v = ml[i];
     const float w = v.y * exp2f(v.x - big);
     tot += w;
@@ -482,8 +486,25 @@ __global__ void __launch_bounds__(128) decode_reduce_kernel(const DecodeParams p
 #pragma unroll
     for (int d = 0; d < DPL; ++d) acc[d] = fmaf(w, of[d], acc[d]);
   }
+  if constexpr (WPH > 1) {
 #pragma unroll
-  for (int d = 0; d < DPL; ++d) out[d] = Elem<T>::from_f(acc[d] / tot);
+    for (int d = 0; d < DPL; ++d) part_acc[warp][lane * DPL + d] = acc[d];
+    if (lane == 0) part_tot[warp] = tot;
+    __syncthreads();
+    if (sub == 0) {
+#pragma unroll
+      for (int w = 1; w < WPH; ++w) tot += part_tot[warp + w];
+#pragma unroll
+      for (int d = 0; d < DPL; ++d)
+#pragma unroll
+        for (int w = 1; w < WPH; ++w) acc[d] += part_acc[warp + w][lane * DPL + d];
+    }
+  }
+  if (!live || sub != 0) return;
+  T* out = static_cast<T*>(p.out) + ((int64_t)s * p.num_heads + h) * D + lane * DPL;
+#pragma unroll
+  for (int d = 0; d < DPL; ++d)
+    out[d] = Elem<T>::from_f(bad ? 0.f : acc[d] / tot);  // a bad partition zeroes the row
 }
 
 }  // namespace pkv

@@ -60,8 +60,13 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* map
     kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
   }
   if (p.num_parts > 1) {
-    dim3 g2((unsigned)((p.num_heads + 3) / 4), (unsigned)num_seqs);
-    decode_reduce_kernel<T, D><<<g2, 128, 0, stream>>>(p);
+    if (p.num_parts <= 8) {
+      dim3 g2((unsigned)((p.num_heads + kReduceWarps - 1) / kReduceWarps), (unsigned)num_seqs);
+      decode_reduce_kernel<T, D, 1><<<g2, kReduceWarps * 32, 0, stream>>>(p);
+    } else {
+      dim3 g2((unsigned)p.num_heads, (unsigned)num_seqs);
+      decode_reduce_kernel<T, D, kReduceWarps><<<g2, kReduceWarps * 32, 0, stream>>>(p);
+    }
   }
   return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
