@@ -47,8 +47,8 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
 # hash of the kernel sources they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b": (1280282888, "b57d4f0a238e7471"),
-    "gqa": (1124731408, "b57d4f0a238e7471"),
+    "opt13b": (1280290784, "29e456e9784abf13"),
+    "gqa": (1128956920, "29e456e9784abf13"),
 }
 
 
