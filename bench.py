@@ -73,12 +73,21 @@ def hbm_peak():
 # workload (product side: the native block manager plans the step)
 # ---------------------------------------------------------------------------
 class Workload:
-    def __init__(self, name, rank=0):
+    """One decode step of a named workload, planned by the native block manager.
+
+    ``block_size`` overrides the workload's block size; ``table="identity"``
+    hands out physical blocks in order (each sequence's blocks contiguous and
+    sequences back to back) instead of from a shuffled free list, which
+    isolates the cost of scattered pages from the rest of the paging.
+    """
+
+    def __init__(self, name, rank=0, block_size=None, table="shuffled"):
         import paged_kv_cache_145_gb300 as pkv
 
         cfg = synth.CONFIGS[name]
         self.name, self.cfg = name, cfg
-        self.b = b = cfg["block_size"]
+        self.b = b = block_size or cfg["block_size"]
+        self.table_kind = table
         self.H, self.Hk, self.D, self.dtype = cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
         self.elt = synth.ELEM_BYTES[self.dtype]
         ceil_div = lambda a, c: -(-a // c)  # noqa: E731
@@ -91,7 +100,9 @@ class Workload:
             self.ids = list(range(len(lengths)))
             need = sum(ceil_div(int(t) + 1, b) for t in lengths)
         self.N = cfg.get("pool_blocks") or synth.pool_with_slack(need, cfg["slack"])
-        bm = pkv.BlockManager(self.N, b, synth.free_order(synth.seed_of(name, 2) + rank, self.N))
+        order = (np.arange(self.N, dtype=np.int64) if table == "identity"
+                 else synth.free_order(synth.seed_of(name, 2) + rank, self.N))
+        bm = pkv.BlockManager(self.N, b, order)
         if name == "fork":
             for i in range(g):
                 bm.admit(i * f, prompt)
@@ -105,6 +116,9 @@ class Workload:
         self.tables, self.seq_lens = bm.tables(self.ids, self.max_blocks)
         self.S = len(self.ids)
         self.max_len = int(self.seq_lens.max())
+        # Stored positions over allocated slots (tail waste of the last blocks).
+        self.utilization = float(self.seq_lens.sum()) / float(b * sum(
+            bm.num_seq_blocks(i) for i in self.ids))
 
     # Algorithmic bytes, counted without reuse across sequences.
     def decode_bytes(self, part):
@@ -325,7 +339,7 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_timed(args.config, args.cpu_budget)
 
-    w = Workload(args.config, rank=rank)
+    w = Workload(args.config, rank=rank, block_size=args.block_size or None, table=args.table)
     dt = synth.TORCH_DTYPE[w.dtype]
     seed = synth.seed_of(args.config, 3) + 10 * rank
     shape = (w.N, w.Hk, w.b, w.D)
@@ -441,7 +455,8 @@ def run_ours(args):
         "data": "synthetic",
         "config": {"workload": args.config, "about": w.cfg["about"], "num_seqs": w.S,
                    "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
-                   "pool_blocks": w.N, "partition_size": part,
+                   "pool_blocks": w.N, "partition_size": part, "table": w.table_kind,
+                   "slot_utilization": round(w.utilization, 5),
                    "l2": "no flush: the %.2f GB pool read per step exceeds the 129 MB L2"
                          % (kv_bytes / 1e9),
                    "parallelism": "replicas" if world > 1 else "single"},
@@ -475,6 +490,9 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--config", default="opt13b", choices=sorted(k for k in synth.CONFIGS if k != "tiny"))
     ap.add_argument("--partition", type=int, default=0, help="positions per partition (0 = default)")
+    ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
+    ap.add_argument("--table", choices=("shuffled", "identity"), default="shuffled",
+                    help="physical block order: shuffled pool (default) or consecutive blocks")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

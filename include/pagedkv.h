@@ -74,7 +74,7 @@ typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
 #define PKV_DEV_PAIR_RANGE   8u  /* paged_block_copy: src or dst not in [0, N)    */
 #define PKV_DEV_TIMEOUT     16u  /* a bounded wait for a bulk copy gave up        */
 
-/* The paged pool.  Supported geometry: block_size in {8, 16, 32},
+/* The paged pool.  Supported geometry: block_size in {8, 16, 32, 64},
  * head_dim in {64, 128}.  k_cache / v_cache must be 16-byte aligned. */
 typedef struct {
   void*   k_cache;       /* [num_blocks][num_kv_heads][block_size][head_dim] */

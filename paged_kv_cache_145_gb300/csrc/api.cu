@@ -56,7 +56,8 @@ int check_cache(const pkv_cache* c) {
 
 bool decode_geometry_ok(const pkv_cache* c, int num_heads) {
   if (c->head_dim != 64 && c->head_dim != 128) return false;
-  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32) return false;
+  if (c->block_size != 8 && c->block_size != 16 && c->block_size != 32 && c->block_size != 64)
+    return false;
   if (num_heads < 1 || num_heads % c->num_kv_heads) return false;
   const int g = num_heads / c->num_kv_heads;
   return g == 1 || g == 2 || g == 4 || g == 8;
@@ -98,11 +99,10 @@ WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_len
 }
 
 // The tensor-core decode kernel serves fp16 / bf16 pools whose query heads
-// come in groups of 2, 4 or 8 and whose blocks hold a multiple of 16
-// positions.  PKV_DECODE_KERNEL=simt in the environment selects the
+// come in groups of 2, 4 or 8 (any supported block size).  PKV_DECODE_KERNEL=simt in the environment selects the
 // CUDA-core kernel instead (read on every call).
 bool use_mma(const pkv_cache* c, int group) {
-  if (c->dtype == PKV_F32 || group < 2 || c->block_size % 16) return false;
+  if (c->dtype == PKV_F32 || group < 2) return false;
   const char* env = std::getenv("PKV_DECODE_KERNEL");
   return !(env && std::strcmp(env, "simt") == 0);
 }
@@ -121,7 +121,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Describes a [N][Hk][b][D] pool as a 4-D tensor (D fastest) read in boxes of
-// 16 rows x 64 elements (128 bytes) with the 128-byte shared-memory swizzle.
+// min(b, 16) rows x 64 elements (128 bytes) with the 128-byte shared-memory
+// swizzle.
 bool encode_pool_map(CUtensorMap* map, const pkv_cache* c, void* base) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -130,7 +131,7 @@ bool encode_pool_map(CUtensorMap* map, const pkv_cache* c, void* base) {
                               (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->num_blocks};
   const cuuint64_t strides[3] = {c->head_dim * elt, c->block_size * c->head_dim * elt,
                                  (cuuint64_t)c->num_kv_heads * c->block_size * c->head_dim * elt};
-  const cuuint32_t box[4] = {64, 16, 1, 1};
+  const cuuint32_t box[4] = {64, (cuuint32_t)(c->block_size < 16 ? c->block_size : 16), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty =
       c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;

@@ -19,7 +19,7 @@ struct DecodeMaps {
 
 template <typename T, int D, int BS, int G>
 constexpr bool mma_eligible() {
-  return !std::is_same<T, float>::value && G >= 2 && BS % 16 == 0;
+  return !std::is_same<T, float>::value && G >= 2 && BS % 8 == 0;
 }
 
 // One flag word per kernel configuration (`Tag`): kernels of one signature
@@ -90,6 +90,7 @@ int launch_decode_b(const DecodeParams& p, int num_seqs, int block_size, int gro
     case 8: return launch_decode_g<T, D, 8>(p, num_seqs, group, maps, stream);
     case 16: return launch_decode_g<T, D, 16>(p, num_seqs, group, maps, stream);
     case 32: return launch_decode_g<T, D, 32>(p, num_seqs, group, maps, stream);
+    case 64: return launch_decode_g<T, D, 64>(p, num_seqs, group, maps, stream);
   }
   return PKV_ERR_GEOMETRY;
 }

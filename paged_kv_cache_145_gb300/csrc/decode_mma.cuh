@@ -105,7 +105,9 @@ struct MmaCfg {
   static constexpr int kWarps = 4;
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kChunk = 16;                     // positions per MMA tile
-  static constexpr int kChunksPerBlock = BS / kChunk;
+  static constexpr int kBoxRows = BS < 16 ? BS : 16;    // rows per TMA box
+  static constexpr int kBoxesPerChunk = kChunk / kBoxRows;  // blocks a chunk spans
+  static constexpr int kChunksPerBlock = BS < 16 ? 1 : BS / kChunk;
   static constexpr int kCols = D / 64;                  // 128-byte column boxes per row
   static constexpr int kBoxBytes = kChunk * 128;        // 16 rows x 128 B
   static constexpr int kTileBytes = kCols * kBoxBytes;  // one chunk of K (or V)
@@ -119,7 +121,8 @@ struct MmaCfg {
   static constexpr int kAlign = 1024;                   // 128-byte swizzle atom
   static constexpr int kMergeBytes = (kWarps * G * D + 3 * kWarps * G + 2 * G) * 4;
   static_assert(kMergeBytes <= kRingBytes, "merge scratch must fit in the ring");
-  static_assert(BS % kChunk == 0 && D % 64 == 0 && G <= 8, "tensor-core geometry");
+  static_assert((BS % kChunk == 0 || kChunk % BS == 0) && D % 64 == 0 && G <= 8,
+                "tensor-core geometry");
   static constexpr int smem_bytes(int part_size) {
     return kAlign + kTableOff + (part_size / BS) * 4;
   }
@@ -135,7 +138,6 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
   constexpr int C = Cfg::kChunk;
   constexpr int NW = Cfg::kWarps;
   constexpr int NST = Cfg::kStages;
-  constexpr int CPB = Cfg::kChunksPerBlock;
   constexpr int KSTEPS = D / 16;
   constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -209,19 +211,30 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
   const uint32_t bar0 = smem_addr(&bars[warp * NST]);
   const uint64_t policy = policy_evict_first();
 
+  // Chunk c covers partition positions 16c .. 16c+15.  With b >= 16 that is
+  // 16 rows of one block; with b = 8 it is two whole blocks,
+  // loaded as two 8-row boxes stacked in shared memory (the same swizzled
+  // layout as one 16-row box).  A second block past the partition's end is
+  // not loaded; its rows are masked (K) and zeroed (V) like any tail.
   auto issue = [&](int j) {
     const int c = warp + j * NW;
     const int st = j % NST;
-    const int pb = stable[c / CPB];
-    const int row = (c % CPB) * C;
     const uint32_t bar = bar0 + st * 8;
     const uint32_t dst = ring0 + st * Cfg::kStageBytes;
-    mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
+    constexpr int RB = Cfg::kBoxRows;
+    int nbox = 1;
+    if constexpr (Cfg::kBoxesPerChunk > 1) nbox = (c * C + RB < ntok) ? 2 : 1;
+    mbar_arrive_expect_tx(bar, nbox * (Cfg::kStageBytes / Cfg::kBoxesPerChunk));
+    for (int hb = 0; hb < nbox; ++hb) {
+      const int pos = c * C + hb * RB;  // first position of this box in the partition
+      const int pb = stable[pos / BS];
+      const int row = pos % BS;
 #pragma unroll
-    for (int cb = 0; cb < Cfg::kCols; ++cb) {
-      tma_load_4d(dst + cb * Cfg::kBoxBytes, &tmk, cb * 64, row, kvh, pb, bar, policy);
-      tma_load_4d(dst + Cfg::kTileBytes + cb * Cfg::kBoxBytes, &tmv, cb * 64, row, kvh, pb, bar,
-                  policy);
+      for (int cb = 0; cb < Cfg::kCols; ++cb) {
+        const uint32_t o = cb * Cfg::kBoxBytes + hb * RB * 128;
+        tma_load_4d(dst + o, &tmk, cb * 64, row, kvh, pb, bar, policy);
+        tma_load_4d(dst + Cfg::kTileBytes + o, &tmv, cb * 64, row, kvh, pb, bar, policy);
+      }
     }
   };
   if (lane == 0) {

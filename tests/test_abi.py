@@ -85,6 +85,7 @@ def test_decode_argument_errors(lib):
     assert decode(lib, c, heads=4 * 3) == -2               # group of 3 unsupported
     assert decode(lib, fake_cache(head_dim=96)) == -2
     assert decode(lib, fake_cache(block_size=4)) == -2
+    assert decode(lib, fake_cache(block_size=128)) == -2
     assert decode(lib, c, part=24) == -3                   # not a multiple of b
     assert decode(lib, c, part=16384) == -3
     assert decode(lib, c, max_len=8 * 16 + 1) == -3        # beyond the table

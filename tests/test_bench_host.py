@@ -57,3 +57,13 @@ def test_combine_ranks_two_gloo_ranks():
     results = mgr.dict()
     tmp.spawn(_rank, args=(2, port, results), nprocs=2, join=True)
     assert results[0] == results[1] == (3000.0, 1.5)
+
+
+def test_slot_utilization_matches_oracle_closed_form():
+    # The bench's utilization (positions over allocated slots, from the native
+    # block manager) equals the oracle's sum(T) / sum(b * ceil(T / b)).
+    for b in (8, 16, 32, 64):
+        for table in ("shuffled", "identity"):
+            w = bench.Workload("opt13b", block_size=b, table=table)
+            lens = [int(x) for x in w.seq_lens]
+            assert abs(w.utilization - float(P.paged_utilization(lens, b))) < 1e-12

@@ -67,6 +67,8 @@ GRID = [(dt, D, b, G, part)
         for part in (0, 2)]
 GRID += [("f16", 128, 16, 2, 0), ("f16", 128, 16, 8, 0), ("bf16", 128, 16, 8, 2),
          ("bf16", 64, 8, 2, 2), ("f32", 128, 32, 8, 0)]
+GRID += [(dt, 128, 64, G, part) for dt in ("f16", "bf16") for G in (1, 4) for part in (0, 2)]
+GRID += [("f32", 64, 64, 2, 2)]
 
 
 @pytest.fixture(params=["auto", "simt"])
@@ -236,17 +238,18 @@ def test_empty_batch_is_a_no_op():
     assert out.shape == (0, 4, 64) and pkv.paged_get_device_error() == 0
 
 
-@pytest.mark.parametrize("dt,G", [("bf16", 4), ("f16", 8), ("f16", 1), ("f32", 4)])
-def test_stale_nan_slots_never_reach_the_output(dt, G, kernel):
+@pytest.mark.parametrize("dt,G,b", [("bf16", 4, 16), ("f16", 8, 16), ("f16", 1, 16), ("f32", 4, 16),
+                                    ("bf16", 4, 8), ("f16", 2, 32), ("bf16", 8, 64)])
+def test_stale_nan_slots_never_reach_the_output(dt, G, b, kernel):
     # Slots past each sequence's end inside its last block hold NaN; the
     # kernels must neither use them nor let 0 * NaN into the sums.
-    lens = [1, 5, 16, 17, 31, 250]
-    c = Case(dt, 2 * G, 2, 128, 16, lens, seed=13)
+    lens = [1, 5, 8, 9, 16, 17, 31, 250]
+    c = Case(dt, 2 * G, 2, 128, b, lens, seed=13)
     for s_, L in enumerate(lens):
-        last = int(c.tables[s_, (L - 1) // 16])
-        c.k[last, :, (L - 1) % 16 + 1:] = float("nan")
-        c.v[last, :, (L - 1) % 16 + 1:] = float("nan")
-    out, err = c.gpu(part=32)
+        last = int(c.tables[s_, (L - 1) // b])
+        c.k[last, :, (L - 1) % b + 1:] = float("nan")
+        c.v[last, :, (L - 1) % b + 1:] = float("nan")
+    out, err = c.gpu(part=max(32, 2 * b))  # several partitions, each a multiple of b
     assert err == 0
     got = gpu_out_f64(out)
     ref, _ = c.oracle()
