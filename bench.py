@@ -482,6 +482,113 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# data-movement kernels at bandwidth-sized launches (--op write|copy|swap)
+# ---------------------------------------------------------------------------
+def _timed(fn, steps, warmup, stream):
+    import torch
+
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for a, z in evs:
+        a.record(stream)
+        fn()
+        z.record(stream)
+    torch.cuda.synchronize()
+    return statistics.fmean(a.elapsed_time(z) for a, z in evs) / 1e3
+
+
+def run_op(args):
+    """Bandwidth of the KV write, block copy or block swap at sizes of our
+    choosing (a decode step's write and copies are too small to time for
+    bandwidth): every cached position written once; half the pool copied to
+    the other half by shuffled disjoint pairs; half the pool swapped out to
+    pinned host memory and back."""
+    import torch
+
+    import paged_kv_cache_145_gb300 as pkv
+
+    rank, local_rank, world = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = Workload(args.config, block_size=args.block_size or None, table=args.table)
+    seed = synth.seed_of(args.config, 3)
+    shape = (w.N, w.Hk, w.b, w.D)
+    cache = pkv.PagedKVCache(synth.normal(seed, shape, w.dtype, device="cuda"),
+                             synth.normal(seed + 1, shape, w.dtype, device="cuda"))
+    stream = torch.cuda.current_stream()
+    block_bytes = w.Hk * w.b * w.D * w.elt
+    peak, peak_kind = hbm_peak()
+    extra = {}
+    if args.op == "write":
+        # Slots of every cached position of every sequence, through its table.
+        t = [np.arange(L) for L in w.seq_lens]
+        slots = np.concatenate([w.tables[i][ti // w.b].astype(np.int64) * w.b + ti % w.b
+                                for i, ti in enumerate(t)])
+        n = len(slots)
+        k = synth.normal(seed + 2, (n, w.Hk, w.D), w.dtype, device="cuda")
+        v = synth.normal(seed + 3, (n, w.Hk, w.D), w.dtype, device="cuda")
+        sl = torch.from_numpy(slots).to(dev)
+        secs = _timed(lambda: pkv.paged_kv_write(cache, k, v, sl), args.steps, args.warmup, stream)
+        nbytes = 2 * 2 * n * w.Hk * w.D * w.elt + 8 * n
+        metric, unit_count, kernel = "paged KV write GB/s (prefill-sized)", n, "kv_write_kernel"
+        extra["tokens"] = n
+    elif args.op == "copy":
+        perm = synth.free_order(seed + 4, w.N)
+        half = w.N // 2
+        pairs = torch.from_numpy(np.stack([perm[:half], perm[half:2 * half]], 1)).to(dev)
+        secs = _timed(lambda: pkv.paged_block_copy(cache, pairs), args.steps, args.warmup, stream)
+        nbytes = 2 * 2 * half * block_bytes + 16 * half
+        metric, unit_count, kernel = "paged block copy GB/s (half the pool)", half, "block_move_kernel"
+        extra["pairs"] = half
+    else:
+        half = w.N // 2
+        hk = torch.empty((half, w.Hk, w.b, w.D), dtype=synth.TORCH_DTYPE[w.dtype]).pin_memory()
+        hv = torch.empty_like(hk).pin_memory()
+        perm = synth.free_order(seed + 4, w.N)
+        out_pairs = torch.from_numpy(np.stack([perm[:half], np.arange(half)], 1)).to(dev)
+        in_pairs = torch.from_numpy(np.stack([np.arange(half), perm[:half]], 1)).to(dev)
+        t_out = _timed(lambda: pkv.paged_block_swap(cache, hk, hv, out_pairs, pkv.PKV_SWAP_OUT),
+                       args.steps, args.warmup, stream)
+        t_in = _timed(lambda: pkv.paged_block_swap(cache, hk, hv, in_pairs, pkv.PKV_SWAP_IN),
+                      args.steps, args.warmup, stream)
+        moved = 2 * half * block_bytes
+        # Denominator: the copy engines moving the same bytes as one plain
+        # contiguous cudaMemcpyAsync each way.
+        dbuf = torch.empty(moved, dtype=torch.uint8, device=dev)
+        hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+        c_out = _timed(lambda: hbuf.copy_(dbuf, non_blocking=True), args.steps, args.warmup, stream)
+        c_in = _timed(lambda: dbuf.copy_(hbuf, non_blocking=True), args.steps, args.warmup, stream)
+        secs = (t_out + t_in) / 2
+        nbytes = moved + 16 * half
+        peak = moved / ((c_out + c_in) / 2) / 1e9
+        peak_kind = "measured in this run: contiguous cudaMemcpyAsync of the same bytes"
+        metric, unit_count, kernel = "block swap GB/s (HBM <-> pinned host, half the pool)", half, "block_move_kernel"
+        extra.update(swap_out_gbs=round(moved / t_out / 1e9, 2), swap_in_gbs=round(moved / t_in / 1e9, 2),
+                     memcpy_d2h_gbs=round(moved / c_out / 1e9, 2), memcpy_h2d_gbs=round(moved / c_in / 1e9, 2),
+                     pairs=half)
+    assert pkv.paged_get_device_error() == 0
+    achieved = nbytes / secs / 1e9
+    line = {
+        "metric": metric, "value": round(achieved, 3), "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(secs * 1e3, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic",
+        "config": dict(workload=args.config, op=args.op, block_size=w.b, pool_blocks=w.N,
+                       block_bytes=block_bytes, **extra),
+        "roofline": {"bound": "hbm" if args.op != "swap" else "host-link", "achieved": round(achieved, 2),
+                     "peak": round(peak, 2), "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": None, "kernel": kernel, "peak_source": peak_kind},
+        "gpu_launches": args.steps * (2 if args.op == "swap" else 1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -493,6 +600,9 @@ def main():
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
     ap.add_argument("--table", choices=("shuffled", "identity"), default="shuffled",
                     help="physical block order: shuffled pool (default) or consecutive blocks")
+    ap.add_argument("--op", choices=("step", "write", "copy", "swap"), default="step",
+                    help="step: the decode step (default); write/copy/swap: bandwidth of the KV "
+                         "write, block copy or host swap at sizes of our choosing")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -500,6 +610,8 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op != "step":
+        run_op(args)
     else:
         run_ours(args)
 

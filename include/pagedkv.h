@@ -232,6 +232,36 @@ int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs,
                      int64_t num_pairs, cudaStream_t stream);
 
 /*
+ * paged_block_swap -- move whole blocks between the device pool and a pool in
+ * pinned host memory (keys and values, every KV head):
+ *     PKV_SWAP_OUT:  host block dst := device block src
+ *     PKV_SWAP_IN:   device block dst := host block src
+ *
+ * The swap alternative to recomputation when blocks run out: [VM-LLM]
+ * preemption paragraph (KV data swapped into CPU memory and restored
+ * later) and [vLLM-TGI] "Read the vLLM 0.11.0 scheduler..." (swapping costs
+ * the cache bytes in both directions over the link).  Which sequences to
+ * evict, and the tables that point at swapped-out blocks, are the caller's.
+ *
+ *   host_k, host_v  pinned (page-locked) or managed host memory,
+ *                   [host_blocks][num_kv_heads][block_size][head_dim] of the
+ *                   cache dtype, 16-byte aligned; the kernel reads or writes
+ *                   them directly over the host link
+ *   src_dst_pairs   device, int64[num_pairs][2] as (src, dst)
+ *   direction       PKV_SWAP_OUT or PKV_SWAP_IN
+ *
+ * Pairs naming a block outside its pool are skipped and set
+ * PKV_DEV_PAIR_RANGE.  Destinations must be distinct.  Host memory that is
+ * neither page-locked nor managed returns PKV_ERR_ARG.  The host pool must
+ * not be touched by the CPU until the stream has passed this call.
+ */
+#define PKV_SWAP_OUT 0
+#define PKV_SWAP_IN  1
+int paged_block_swap(const pkv_cache* cache, void* host_k, void* host_v, int64_t host_blocks,
+                     const int64_t* src_dst_pairs, int64_t num_pairs, int32_t direction,
+                     cudaStream_t stream);
+
+/*
  * paged_get_device_error -- synchronise `stream`, then read and clear the
  * current device's error word (an OR of PKV_DEV_* bits; 0 = no error).
  * The word is shared by every stream on the device.

@@ -110,6 +110,35 @@ def copy_blocks(k_pool, v_pool, pairs):
     return k_out, v_out, bad
 
 
+def swap_blocks(dev_k, dev_v, host_k, host_v, pairs, direction):
+    """Move whole blocks between a device pool and a host pool.
+
+    "vLLM and PagedAttention: Virtual Memory for LLM Serving" (preemption
+    paragraph): KV data can be swapped into CPU memory and restored later.
+    ``direction`` "out": host block dst := device block src; "in": device
+    block dst := host block src.  Both pools are ``[blocks, Hk, b, D]``.
+    Pairs naming a block outside its pool are skipped and reported.
+    Returns ``(dev_k', dev_v', host_k', host_v', bad)``.
+    """
+    dk, dv = np.array(dev_k, copy=True), np.array(dev_v, copy=True)
+    hk, hv = np.array(host_k, copy=True), np.array(host_v, copy=True)
+    if direction == "out":
+        src_k, src_v, dst_k, dst_v = dk, dv, hk, hv
+    elif direction == "in":
+        src_k, src_v, dst_k, dst_v = hk, hv, dk, dv
+    else:
+        raise ValueError("direction must be 'out' or 'in'")
+    bad = []
+    for i, (src, dst) in enumerate(pairs):
+        src, dst = int(src), int(dst)
+        if not (0 <= src < src_k.shape[0] and 0 <= dst < dst_k.shape[0]):
+            bad.append(i)
+            continue
+        dst_k[dst] = src_k[src]
+        dst_v[dst] = src_v[src]
+    return dk, dv, hk, hv, bad
+
+
 # ---------------------------------------------------------------------------
 # Attention
 # ---------------------------------------------------------------------------

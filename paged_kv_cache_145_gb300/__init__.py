@@ -18,14 +18,15 @@ import torch
 
 from . import _lib
 from ._lib import (PKV_DEV_PAIR_RANGE, PKV_DEV_SEQ_LEN, PKV_DEV_SLOT_RANGE,  # noqa: F401
-                   PKV_DEV_TABLE_RANGE, PKV_DEV_TIMEOUT, PKV_ERR_NOMEM)
+                   PKV_DEV_TABLE_RANGE, PKV_DEV_TIMEOUT, PKV_ERR_NOMEM, PKV_SWAP_IN,
+                   PKV_SWAP_OUT)
 
 _DTYPE_CODE = {torch.float32: _lib.PKV_F32, torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16}
 
 __all__ = [
     "PagedKVCache", "BlockManager", "paged_kv_write", "paged_attention_decode",
     "paged_attention_workspace_bytes", "paged_attention_partition_size",
-    "paged_block_copy", "paged_get_device_error", "library_path",
+    "paged_block_copy", "paged_block_swap", "paged_get_device_error", "library_path",
 ]
 
 
@@ -151,6 +152,31 @@ def paged_block_copy(cache, pairs, stream=None):
     n = pairs.shape[0] if pairs.numel() else 0
     _lib.check(_lib.lib().paged_block_copy(cache.ref, _ptr(pairs), n, _stream(stream)),
                "paged_block_copy")
+
+
+def paged_block_swap(cache, host_k, host_v, pairs, direction, stream=None):
+    """Move blocks between the device pool and a pinned host pool.
+
+    ``host_k``/``host_v``: pinned CPU tensors ``[M, Hk, b, D]`` of the cache
+    dtype; ``pairs``: int64 ``[n, 2]`` on the device as (src, dst);
+    ``direction``: ``PKV_SWAP_OUT`` (device -> host) or ``PKV_SWAP_IN``.
+    """
+    for t, name in ((host_k, "host_k"), (host_v, "host_v")):
+        if not isinstance(t, torch.Tensor) or t.is_cuda or not t.is_pinned():
+            raise ValueError("%s must be a pinned CPU tensor" % name)
+        if not t.is_contiguous() or t.dtype != cache.dtype:
+            raise ValueError("%s must be contiguous with the cache dtype" % name)
+        if t.dim() != 4 or tuple(t.shape[1:]) != (cache.num_kv_heads, cache.block_size, cache.head_dim):
+            raise ValueError("%s must be [M, kv_heads, block_size, head_dim]" % name)
+    if host_k.shape != host_v.shape:
+        raise ValueError("host_k and host_v must have one shape")
+    _need(pairs, "pairs", torch.int64, cache.device)
+    if pairs.numel() and (pairs.dim() != 2 or pairs.shape[1] != 2):
+        raise ValueError("pairs must be [num_pairs, 2]")
+    n = pairs.shape[0] if pairs.numel() else 0
+    _lib.check(_lib.lib().paged_block_swap(cache.ref, _ptr(host_k), _ptr(host_v), host_k.shape[0],
+                                           _ptr(pairs), n, int(direction), _stream(stream)),
+               "paged_block_swap")
 
 
 def paged_get_device_error(stream=None):

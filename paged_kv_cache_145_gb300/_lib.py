@@ -21,6 +21,7 @@ PKV_DEV_TIMEOUT = 16
 PKV_ERR_WORKSPACE = -5
 PKV_ERR_NOMEM = -8
 PKV_STATIC_WS_BYTES = 32 << 20
+PKV_SWAP_OUT, PKV_SWAP_IN = 0, 1
 
 
 class pkv_cache(ctypes.Structure):
@@ -50,6 +51,7 @@ SIGNATURES = {
     "paged_attention_decode_static_ws": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
                                                         ctypes.c_float, _P, _I32, _P]),
     "paged_block_copy": (ctypes.c_int, [_CACHE, _P, _I64, _P]),
+    "paged_block_swap": (ctypes.c_int, [_CACHE, _P, _P, _I64, _P, _I64, _I32, _P]),
     "paged_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "paged_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_bm_create": (_P, [_I64, _I32, _P]),

@@ -13,6 +13,9 @@ int pkv_launch_kv_write(const pkv_cache* c, const void* k, const void* v, const 
                         int64_t num_tokens, size_t elem_bytes, cudaStream_t stream);
 int pkv_launch_block_copy(const pkv_cache* c, const int64_t* pairs, int64_t num_pairs,
                           size_t elem_bytes, cudaStream_t stream);
+int pkv_launch_block_swap(const pkv_cache* c, void* host_k, void* host_v, int64_t host_blocks,
+                          const int64_t* pairs, int64_t num_pairs, int direction,
+                          size_t elem_bytes, cudaStream_t stream);
 int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
                           cudaStream_t);
 int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
@@ -267,6 +270,43 @@ int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs, int64
     return PKV_ERR_GEOMETRY;
   if (!pkv_error_word()) return PKV_ERR_CUDA;
   return pkv_launch_block_copy(cache, src_dst_pairs, num_pairs, elem_bytes(cache->dtype), stream);
+}
+
+// Device-side address of a host pool, or nullptr if the memory is neither
+// page-locked nor managed (the kernel could not reach it).
+static void* host_pool_address(void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error of the query
+    return nullptr;
+  }
+  if (a.type == cudaMemoryTypeHost) return a.devicePointer;
+  if (a.type == cudaMemoryTypeManaged) return p;
+  return nullptr;
+}
+
+int paged_block_swap(const pkv_cache* cache, void* host_k, void* host_v, int64_t host_blocks,
+                     const int64_t* src_dst_pairs, int64_t num_pairs, int32_t direction,
+                     cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_pairs < 0 || num_pairs > INT32_MAX || host_blocks < 1 ||
+      (direction != PKV_SWAP_OUT && direction != PKV_SWAP_IN))
+    return PKV_ERR_ARG;
+  if (num_pairs == 0) return PKV_OK;
+  if (!host_k || !host_v || !src_dst_pairs) return PKV_ERR_NULL;
+  if (!aligned16(host_k) || !aligned16(host_v) ||
+      (reinterpret_cast<uintptr_t>(src_dst_pairs) & 7u))
+    return PKV_ERR_ALIGN;
+  if ((int64_t)cache->num_kv_heads * cache->block_size * cache->head_dim *
+          (int64_t)elem_bytes(cache->dtype) % 16)
+    return PKV_ERR_GEOMETRY;
+  void* dk = host_pool_address(host_k);
+  void* dv = host_pool_address(host_v);
+  if (!dk || !dv) return PKV_ERR_ARG;
+  if (!pkv_error_word()) return PKV_ERR_CUDA;
+  return pkv_launch_block_swap(cache, dk, dv, host_blocks, src_dst_pairs, num_pairs, direction,
+                               elem_bytes(cache->dtype), stream);
 }
 
 int paged_get_device_error(cudaStream_t stream, uint32_t* bits) {

@@ -415,3 +415,27 @@ def check_bf16(to_f64, seed=9):
     assert np.array_equal(to_f64(bits, "bf16"), ref)
     half = np.random.default_rng(seed).standard_normal(100).astype(np.float16)
     assert np.array_equal(to_f64(half, "f16"), half.astype(np.float64))
+
+
+def check_swap(swap_blocks, copy_blocks, seed=10):
+    """Swapping out then in restores blocks; it equals a copy within one
+    pool made of the device pool followed by the host pool."""
+    rng = np.random.default_rng(seed)
+    dk = rng.integers(0, 2 ** 16, size=(6, 2, 4, 8)).astype(np.uint16)
+    dv = rng.integers(0, 2 ** 16, size=(6, 2, 4, 8)).astype(np.uint16)
+    hk = np.zeros((4, 2, 4, 8), dtype=np.uint16)
+    hv = np.zeros((4, 2, 4, 8), dtype=np.uint16)
+    out_pairs = [(5, 0), (2, 3), (1, 9)]
+    dk1, dv1, hk1, hv1, bad = swap_blocks(dk, dv, hk, hv, out_pairs, "out")
+    assert bad == [2]
+    assert np.array_equal(dk1, dk) and np.array_equal(dv1, dv)
+    both_k, both_v, _ = copy_blocks(np.concatenate([dk, hk]), np.concatenate([dv, hv]),
+                                    [(s_, 6 + d_) for s_, d_ in out_pairs[:2]])
+    assert np.array_equal(hk1, both_k[6:]) and np.array_equal(hv1, both_v[6:])
+    # Reuse the device blocks, then bring the data back elsewhere.
+    dk2 = dk1.copy()
+    dk2[[5, 2]] = 0
+    dk3, dv3, _, _, bad = swap_blocks(dk2, dv1, hk1, hv1, [(0, 4), (3, 0)], "in")
+    assert bad == []
+    assert np.array_equal(dk3[4], dk[5]) and np.array_equal(dk3[0], dk[2])
+    assert np.array_equal(dv3[4], dv[5]) and np.array_equal(dv3[0], dv[2])

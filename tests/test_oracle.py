@@ -82,3 +82,7 @@ def test_oracle_bruteforce_helper_agrees():
     vals = [[float(x) for x in r] for r in pins.contiguous_rows(vp, tables[0], lens[0], b, 1)]
     qr = [float(x) for x in q[0, 1]]
     assert A.attention_bruteforce(qr, keys, vals, 0.3) == pins.brute(qr, keys, vals, 0.3)
+
+
+def test_swap():
+    pins.check_swap(A.swap_blocks, A.copy_blocks)

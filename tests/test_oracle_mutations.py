@@ -104,3 +104,9 @@ def test_release_ignores_sharing():
     bad = mutant(B.BlockPool, "self.refcount[blk] -= 1\n        if self.refcount[blk] == 0:",
                  "self.refcount[blk] = 0\n        if True:")
     fails(pins.check_pool_vs_contiguous, bad, P.allocated_slots)
+
+
+def test_swap_direction():
+    bad = mutant(A.swap_blocks, 'if direction == "out":', 'if direction == "in":')
+    with pytest.raises((AssertionError, IndexError, ValueError)):
+        pins.check_swap(bad, A.copy_blocks)
