@@ -209,6 +209,48 @@ def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, m
     return out, bad
 
 
+def prefill_attention(q, k_pool, v_pool, tables, seq_lens, query_starts, scale, b, dtype,
+                      seqs=None):
+    """Causal attention of a chunk of new queries per sequence (prefill).
+
+    "vLLM and PagedAttention: Virtual Memory for LLM Serving" (opening
+    paragraph): during prefill all prompt tokens are known, so their queries
+    are processed together; "Inside vLLM and TGI: Paging, Versioned
+    Schedulers and Operations" (launch notes: chunked prefill) splits a long
+    prompt into chunks.  Sequence s holds ``L = seq_lens[s]`` positions after
+    its chunk of ``Q = query_starts[s + 1] - query_starts[s]`` queries was
+    written; query i sits at position ``L - Q + i`` and attends, like a
+    decode query, to positions ``0 .. L - Q + i`` of the sequence:
+
+        out[query_starts[s] + i, h] = attention over the first L - Q + i + 1
+                                      positions (see :func:`attention`)
+
+    ``q``: ``[total queries, H, D]``; pools ``[N, Hk, b, D]``; returns
+    ``out float64 [total queries, H, D]`` (rows of unlisted sequences NaN).
+    """
+    q = np.asarray(q)
+    _, n_heads, dim = q.shape
+    kv_heads = k_pool.shape[1]
+    group = n_heads // kv_heads
+    out = np.full(q.shape, np.nan)
+    n_seq = len(seq_lens)
+    for s in (range(n_seq) if seqs is None else seqs):
+        table = [int(x) for x in tables[s]]
+        length = int(seq_lens[s])
+        q0, q1 = int(query_starts[s]), int(query_starts[s + 1])
+        first = length - (q1 - q0)
+        for kvh in range(kv_heads):
+            keys = to_f64(gather_rows(k_pool, table, length, b, kvh), dtype)
+            vals = to_f64(gather_rows(v_pool, table, length, b, kvh), dtype)
+            for h in range(kvh * group, (kvh + 1) * group):
+                for i in range(q1 - q0):
+                    visible = first + i + 1
+                    z = scale * (keys[:visible] @ to_f64(q[q0 + i, h], dtype))
+                    w = np.exp(z - z.max())
+                    out[q0 + i, h] = (w @ vals[:visible]) / w.sum()
+    return out
+
+
 def partition_stats(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, partition_size, seqs=None):
     """Per-partition softmax statistics of a split-K decode.
 

@@ -439,3 +439,48 @@ def check_swap(swap_blocks, copy_blocks, seed=10):
     assert bad == []
     assert np.array_equal(dk3[4], dk[5]) and np.array_equal(dk3[0], dk[2])
     assert np.array_equal(dv3[4], dv[5]) and np.array_equal(dv3[0], dv[2])
+
+
+def check_prefill(prefill_attention, attention, seed=11):
+    """Prefill pins: a one-query chunk is decode; with no cached prefix and an
+    identity table it is torch's causal scaled-dot-product attention; the
+    outputs of earlier queries do not depend on later keys."""
+    rng = np.random.default_rng(seed)
+    b, hk, G, d = 4, 2, 2, 8
+    lens = [9, 6, 13]
+    chunk = [3, 6, 1]                      # queries per sequence (6 = whole prompt)
+    starts = np.concatenate([[0], np.cumsum(chunk)])
+    nblk = [-(-L // b) for L in lens]
+    perm = rng.permutation(sum(nblk) + 2)
+    tables, pos = [], 0
+    for k in nblk:
+        tables.append([int(x) for x in perm[pos:pos + k]]); pos += k
+    kp = rng.standard_normal((len(perm), hk, b, d)).astype(np.float32)
+    vp = rng.standard_normal((len(perm), hk, b, d)).astype(np.float32)
+    q = rng.standard_normal((int(starts[-1]), hk * G, d)).astype(np.float32)
+    out = prefill_attention(q, kp, vp, tables, lens, starts, 0.35, b, "f32")
+    # One-query chunk (sequence 2) and each query of a chunk = decode over its prefix.
+    for s_ in range(3):
+        for i in range(chunk[s_]):
+            L = lens[s_] - chunk[s_] + i + 1
+            ref, _ = attention(q[starts[s_] + i:starts[s_] + i + 1], kp, vp, [tables[s_]], [L],
+                               0.35, b, "f32")
+            assert np.max(np.abs(out[starts[s_] + i] - ref[0])) < 1e-12
+    # Whole-prompt chunk (sequence 1, no prefix): torch causal attention.
+    rows = lambda pool: np.stack([pool[tables[1][t // b], :, t % b] for t in range(6)])  # noqa: E731
+    kc = torch.from_numpy(rows(kp).astype(np.float64)).permute(1, 0, 2)   # [Hk, 6, d]
+    vc = torch.from_numpy(rows(vp).astype(np.float64)).permute(1, 0, 2)
+    qc = torch.from_numpy(q[starts[1]:starts[2]].astype(np.float64)).permute(1, 0, 2)  # [H, 6, d]
+    kc = kc.repeat_interleave(G, dim=0)
+    vc = vc.repeat_interleave(G, dim=0)
+    ref = torch.nn.functional.scaled_dot_product_attention(qc, kc, vc, is_causal=True, scale=0.35)
+    assert np.max(np.abs(out[starts[1]:starts[2]] - ref.permute(1, 0, 2).numpy())) < 1e-12
+    # Causality: changing the last position's key and value leaves every
+    # query that cannot see it unchanged.
+    k2, v2 = kp.copy(), vp.copy()
+    last = lens[0] - 1
+    k2[tables[0][last // b], :, last % b] += 5.0
+    v2[tables[0][last // b], :, last % b] -= 3.0
+    out2 = prefill_attention(q, k2, v2, tables, lens, starts, 0.35, b, "f32", seqs=[0])
+    assert np.array_equal(out2[starts[0]:starts[0] + 2], out[starts[0]:starts[0] + 2])
+    assert not np.allclose(out2[starts[0] + 2], out[starts[0] + 2])

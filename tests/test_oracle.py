@@ -86,3 +86,7 @@ def test_oracle_bruteforce_helper_agrees():
 
 def test_swap():
     pins.check_swap(A.swap_blocks, A.copy_blocks)
+
+
+def test_prefill():
+    pins.check_prefill(A.prefill_attention, A.attention)

@@ -110,3 +110,14 @@ def test_swap_direction():
     bad = mutant(A.swap_blocks, 'if direction == "out":', 'if direction == "in":')
     with pytest.raises((AssertionError, IndexError, ValueError)):
         pins.check_swap(bad, A.copy_blocks)
+
+
+def test_prefill_not_causal():
+    bad = mutant(A.prefill_attention, "visible = first + i + 1", "visible = length")
+    fails(pins.check_prefill, bad, A.attention)
+
+
+def test_prefill_off_by_one_position():
+    bad = mutant(A.prefill_attention, "visible = first + i + 1", "visible = first + i")
+    with pytest.raises((AssertionError, IndexError, ValueError)):
+        pins.check_prefill(bad, A.attention)
