@@ -501,6 +501,98 @@ def _timed(fn, steps, warmup, stream):
     return statistics.fmean(a.elapsed_time(z) for a, z in evs) / 1e3
 
 
+PREFILL_CONFIGS = ("prefill", "chunked")
+DECODE_CONFIGS = ("opt13b", "gqa", "fork", "long")
+
+
+def run_prefill(args):
+    """Prefill step: write each sequence's chunk of new keys/values, then
+    causal attention of the chunk's queries over prefix + chunk."""
+    import torch
+
+    import paged_kv_cache_145_gb300 as pkv
+
+    rank, local_rank, world = dist_env()
+    if rank != 0:
+        return
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    cfg = synth.CONFIGS[args.config]
+    b, H, Hk, D, dt = cfg["block_size"], cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
+    S, prefix, chunk = cfg["batch"], cfg["prefix"], cfg["chunk"]
+    need = S * (-(-(prefix + chunk) // b))
+    n = synth.pool_with_slack(need, cfg["slack"])
+    bm = pkv.BlockManager(n, b, synth.free_order(synth.seed_of(args.config, 2), n))
+    slots = []
+    for i in range(S):
+        bm.admit(i, prefix + chunk)
+        slots.append(bm.slots(i, prefix, chunk))
+    slots = np.concatenate(slots)
+    width = max(bm.num_seq_blocks(i) for i in range(S))
+    tables, lens = bm.tables(range(S), width)
+    seed = synth.seed_of(args.config, 3)
+    cache = pkv.PagedKVCache(synth.normal(seed, (n, Hk, b, D), dt, device="cuda"),
+                             synth.normal(seed + 1, (n, Hk, b, D), dt, device="cuda"))
+    T = S * chunk
+    q = synth.normal(seed + 2, (T, H, D), dt, device="cuda")
+    k = synth.normal(seed + 3, (T, Hk, D), dt, device="cuda")
+    v = synth.normal(seed + 4, (T, Hk, D), dt, device="cuda")
+    out = torch.empty_like(q)
+    sl = torch.from_numpy(slots).to(dev)
+    starts = torch.arange(0, T + 1, chunk, dtype=torch.int32, device=dev)
+    tab = torch.from_numpy(tables).to(dev)
+    ln = torch.from_numpy(lens).to(dev)
+    scale = 1.0 / math.sqrt(D)
+    stream = torch.cuda.current_stream()
+
+    def step(mid=None):
+        pkv.paged_kv_write(cache, k, v, sl)
+        if mid is not None:
+            mid.record(stream)
+        pkv.paged_attention_prefill(cache, q, starts, tab, ln, scale, chunk, out=out)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pkv.paged_get_device_error() == 0
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    for a, m_, z in evs:
+        a.record(stream)
+        step(m_)
+        z.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    assert pkv.paged_get_device_error() == 0
+    step_s = evs[0][0].elapsed_time(evs[-1][2]) / 1e3 / args.steps
+    attn_s = statistics.fmean(m_.elapsed_time(z) for _, m_, z in evs) / 1e3
+    # Algorithmic FLOPs: QK^T and PV, 2 * D each, per (query, head, visible key).
+    visible = S * sum(prefix + i + 1 for i in range(chunk))
+    flops = 4 * D * H * visible
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            peak, kind = float(json.load(fh)["bf16_tflops"]), "measured cuBLAS bf16 burst"
+    except (OSError, KeyError, ValueError):
+        peak, kind = 1900.0, "fallback"
+    line = {
+        "metric": "paged prefill attention TFLOP/s (causal, GQA)", "value": round(flops / step_s / 1e12, 3),
+        "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": args.config, "about": cfg["about"], "sequences": S, "prefix": prefix,
+                   "chunk": chunk, "pool_blocks": n},
+        "prefill_tokens_per_s": round(T / step_s, 1),
+        "roofline": {"bound": "tensor", "achieved": round(flops / attn_s / 1e12, 2), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(flops / attn_s / 1e12 / peak, 4), "traffic": None,
+                     "kernel": "prefill_mma_kernel (mma.sync m16n8k16)", "peak_source": kind,
+                     "attention_us": round(attn_s * 1e6, 2)},
+        "clocks": clocks, "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_op(args):
     """Bandwidth of the KV write, block copy or block swap at sizes of our
     choosing (a decode step's write and copies are too small to time for
@@ -600,9 +692,10 @@ def main():
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
     ap.add_argument("--table", choices=("shuffled", "identity"), default="shuffled",
                     help="physical block order: shuffled pool (default) or consecutive blocks")
-    ap.add_argument("--op", choices=("step", "write", "copy", "swap"), default="step",
+    ap.add_argument("--op", choices=("step", "write", "copy", "swap", "prefill"), default="step",
                     help="step: the decode step (default); write/copy/swap: bandwidth of the KV "
-                         "write, block copy or host swap at sizes of our choosing")
+                         "write, block copy or host swap at sizes of our choosing; prefill: "
+                         "chunk write + causal prefill attention (--config prefill|chunked)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -610,6 +703,10 @@ def main():
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "prefill" or args.config in PREFILL_CONFIGS:
+        if args.config not in PREFILL_CONFIGS:
+            ap.error("--op prefill needs --config prefill or chunked")
+        run_prefill(args)
     elif args.op != "step":
         run_op(args)
     else:

@@ -180,6 +180,38 @@ int paged_attention_decode(const pkv_cache* cache, const void* q,
                            int32_t partition_size, cudaStream_t stream);
 
 /*
+ * paged_attention_prefill -- causal attention of a chunk of new queries per
+ * sequence through the block tables (prefill and chunked prefill).
+ *
+ * [VM-LLM] opening paragraph: in prefill all prompt tokens are known and
+ * processed together; [vLLM-TGI] launch notes: chunked prefill splits long
+ * prompts.  Sequence s holds L = seq_lens[s] positions, the last
+ * Q = query_starts[s+1] - query_starts[s] of which are its new queries (their
+ * keys and values already written, e.g. by paged_kv_write).  Query i of the
+ * chunk sits at position L - Q + i and attends to positions 0 .. L - Q + i:
+ *     out[query_starts[s] + i][h] = softmax-weighted mean, as in
+ *     paged_attention_decode, over the first L - Q + i + 1 positions
+ * accumulated in float32 on tensor cores.  fp16 and bf16 pools only.
+ *
+ *   q, out        device, [total_queries][num_heads][head_dim], cache dtype
+ *   query_starts  device, int32[num_seqs + 1], non-decreasing, last <=
+ *                 total_queries
+ *   max_queries   host bound on any sequence's Q (sizes the launch)
+ *   block_tables, seq_lens, scale: as for paged_attention_decode
+ *
+ * A sequence whose Q exceeds its length or max_queries, or whose length
+ * exceeds the table, gets zero rows and PKV_DEV_SEQ_LEN; one whose used
+ * table entries leave [0, num_blocks) gets zero rows and
+ * PKV_DEV_TABLE_RANGE.  max_blocks_per_seq is bounded by shared memory
+ * (about 38k entries).
+ */
+int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total_queries,
+                            const int32_t* query_starts, int32_t num_seqs, int32_t max_queries,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t num_heads, float scale, void* out,
+                            cudaStream_t stream);
+
+/*
  * paged_attention_decode_static_ws -- paged_attention_decode without a
  * caller-supplied workspace.  The pages have no counterpart to this call; it
  * exists for callers that cannot allocate device memory themselves (a
@@ -318,6 +350,12 @@ int pkv_bm_release(pkv_block_manager* bm, int64_t seq);
  * than max_blocks. */
 int pkv_bm_tables(const pkv_block_manager* bm, const int64_t* seqs, int64_t n,
                   int32_t max_blocks, int32_t* tables, int32_t* seq_lens);
+
+/* Slots of positions start .. start+count-1 of `seq` (host, int64[count]),
+ * e.g. the slot mapping of a prefill chunk.  PKV_ERR_ARG if the range is not
+ * inside the sequence. */
+int pkv_bm_slots(const pkv_block_manager* bm, int64_t seq, int64_t start, int64_t count,
+                 int64_t* slot_mapping);
 
 int64_t pkv_bm_num_free(const pkv_block_manager* bm);
 int64_t pkv_bm_seq_len(const pkv_block_manager* bm, int64_t seq);     /* -1 if unknown */

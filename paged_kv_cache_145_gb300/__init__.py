@@ -25,6 +25,7 @@ _DTYPE_CODE = {torch.float32: _lib.PKV_F32, torch.float16: _lib.PKV_F16, torch.b
 
 __all__ = [
     "PagedKVCache", "BlockManager", "paged_kv_write", "paged_attention_decode",
+    "paged_attention_prefill",
     "paged_attention_workspace_bytes", "paged_attention_partition_size",
     "paged_block_copy", "paged_block_swap", "paged_get_device_error", "library_path",
 ]
@@ -144,6 +145,35 @@ def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, ma
     return out
 
 
+def paged_attention_prefill(cache, q, query_starts, block_tables, seq_lens, scale, max_queries,
+                            out=None, stream=None):
+    """Causal attention of each sequence's chunk of new queries.
+
+    ``q``: ``[total_queries, H, D]``; ``query_starts``: int32 ``[S + 1]``;
+    ``block_tables``: int32 ``[S, max_blocks]``; ``seq_lens``: int32 ``[S]``
+    (positions including the chunk); ``max_queries``: host bound on any
+    chunk's length.  Returns ``out``.
+    """
+    _need(q, "q", cache.dtype, cache.device)
+    _need(query_starts, "query_starts", torch.int32, cache.device)
+    _need(block_tables, "block_tables", torch.int32, cache.device)
+    _need(seq_lens, "seq_lens", torch.int32, cache.device)
+    if q.dim() != 3 or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be [total_queries, num_heads, head_dim]")
+    num_seqs = seq_lens.shape[0]
+    if query_starts.shape != (num_seqs + 1,) or block_tables.dim() != 2 or \
+            block_tables.shape[0] != num_seqs:
+        raise ValueError("query_starts must be [S + 1] and block_tables [S, max_blocks]")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", cache.dtype, cache.device)
+    _lib.check(_lib.lib().paged_attention_prefill(
+        cache.ref, _ptr(q), q.shape[0], _ptr(query_starts), num_seqs, int(max_queries),
+        _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), q.shape[1], float(scale),
+        _ptr(out), _stream(stream)), "paged_attention_prefill")
+    return out
+
+
 def paged_block_copy(cache, pairs, stream=None):
     """Copy blocks ``pairs[i, 0] -> pairs[i, 1]`` (int64 ``[n, 2]``)."""
     _need(pairs, "pairs", torch.int64, cache.device)
@@ -246,6 +276,12 @@ class BlockManager:
         _lib.check(self._lib.pkv_bm_tables(self._h, s.ctypes.data, s.shape[0], max_blocks,
                                            tab.ctypes.data, lens.ctypes.data), "tables")
         return tab, lens
+
+    def slots(self, seq, start, count):
+        """Slots of positions ``start .. start+count-1`` of a sequence."""
+        out = np.empty(count, dtype=np.int64)
+        _lib.check(self._lib.pkv_bm_slots(self._h, seq, start, count, out.ctypes.data), "slots")
+        return out
 
     def num_free(self):
         return int(self._lib.pkv_bm_num_free(self._h))

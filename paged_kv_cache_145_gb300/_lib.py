@@ -50,6 +50,8 @@ SIGNATURES = {
                                               ctypes.c_float, _P, _P, ctypes.c_size_t, _I32, _P]),
     "paged_attention_decode_static_ws": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
                                                         ctypes.c_float, _P, _I32, _P]),
+    "paged_attention_prefill": (ctypes.c_int, [_CACHE, _P, _I64, _P, _I32, _I32, _P, _I32, _P,
+                                               _I32, ctypes.c_float, _P, _P]),
     "paged_block_copy": (ctypes.c_int, [_CACHE, _P, _I64, _P]),
     "paged_block_swap": (ctypes.c_int, [_CACHE, _P, _P, _I64, _P, _I64, _I32, _P]),
     "paged_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
@@ -61,6 +63,7 @@ SIGNATURES = {
     "pkv_bm_append": (ctypes.c_int, [_P, _P, _I64, _P, _P, ctypes.POINTER(_I64)]),
     "pkv_bm_release": (ctypes.c_int, [_P, _I64]),
     "pkv_bm_tables": (ctypes.c_int, [_P, _P, _I64, _I32, _P, _P]),
+    "pkv_bm_slots": (ctypes.c_int, [_P, _I64, _I64, _I64, _P]),
     "pkv_bm_num_free": (_I64, [_P]),
     "pkv_bm_seq_len": (_I64, [_P, _I64]),
     "pkv_bm_num_seq_blocks": (_I64, [_P, _I64]),

@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "decode_launch.cuh"
+#include "prefill.cuh"
 
 int pkv_launch_kv_write(const pkv_cache* c, const void* k, const void* v, const int64_t* slots,
                         int64_t num_tokens, size_t elem_bytes, cudaStream_t stream);
@@ -16,6 +17,10 @@ int pkv_launch_block_copy(const pkv_cache* c, const int64_t* pairs, int64_t num_
 int pkv_launch_block_swap(const pkv_cache* c, void* host_k, void* host_v, int64_t host_blocks,
                           const int64_t* pairs, int64_t num_pairs, int direction,
                           size_t elem_bytes, cudaStream_t stream);
+int pkv_launch_prefill_f16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
+                           const CUtensorMap&, cudaStream_t);
+int pkv_launch_prefill_bf16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
+                            const CUtensorMap&, cudaStream_t);
 int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
                           cudaStream_t);
 int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
@@ -255,6 +260,55 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
     case PKV_BF16: return pkv_launch_decode_bf16(p, num_seqs, D, B, group, mp, stream);
   }
   return PKV_ERR_ARG;
+}
+
+int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total_queries,
+                            const int32_t* query_starts, int32_t num_seqs, int32_t max_queries,
+                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                            const int32_t* seq_lens, int32_t num_heads, float scale, void* out,
+                            cudaStream_t stream) {
+  int rc = check_cache(cache);
+  if (rc) return rc;
+  if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 1 || num_heads < 1 ||
+      total_queries < 0 || total_queries > INT32_MAX || max_queries < 1 || !std::isfinite(scale))
+    return PKV_ERR_ARG;
+  if (num_seqs == 0 || total_queries == 0) return PKV_OK;
+  if (!q || !out || !query_starts || !block_tables || !seq_lens) return PKV_ERR_NULL;
+  if (cache->dtype == PKV_F32 || !decode_geometry_ok(cache, num_heads)) return PKV_ERR_GEOMETRY;
+  if (cache->num_kv_heads > 65535 || (int64_t)max_blocks_per_seq * cache->block_size > INT32_MAX)
+    return PKV_ERR_ARG;
+  if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_starts) & 3u))
+    return PKV_ERR_ALIGN;
+  // The partition's table entries are staged in shared memory next to a
+  // 64 KiB ring: bound the table width accordingly.
+  if ((int64_t)max_blocks_per_seq * 4 > 150 * 1024) return PKV_ERR_ARG;
+  unsigned* err = pkv_error_word();
+  if (!err) return PKV_ERR_CUDA;
+  CUtensorMap mk, mv;
+  if (!encode_pool_map(&mk, cache, cache->k_cache) || !encode_pool_map(&mv, cache, cache->v_cache))
+    return PKV_ERR_CUDA;
+  pkv::PrefillParams p{};
+  p.q = q;
+  p.out = out;
+  p.starts = query_starts;
+  p.total_queries = total_queries;
+  p.tables = block_tables;
+  p.max_blocks = max_blocks_per_seq;
+  p.seq_lens = seq_lens;
+  p.num_blocks = cache->num_blocks;
+  p.kv_heads = cache->num_kv_heads;
+  p.num_heads = num_heads;
+  p.max_queries = max_queries;
+  p.qscale = scale * 1.4426950408889634f;
+  p.err = err;
+  const int group = num_heads / cache->num_kv_heads;
+  if (cache->dtype == PKV_F16)
+    return pkv_launch_prefill_f16(p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv,
+                                  stream);
+  return pkv_launch_prefill_bf16(p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv,
+                                 stream);
 }
 
 int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs, int64_t num_pairs,

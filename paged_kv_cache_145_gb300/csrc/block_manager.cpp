@@ -202,6 +202,21 @@ int pkv_bm_tables(const pkv_block_manager* bm, const int64_t* seqs, int64_t n, i
   return PKV_OK;
 }
 
+int pkv_bm_slots(const pkv_block_manager* bm, int64_t seq, int64_t start, int64_t count,
+                 int64_t* slot_mapping) {
+  if (!bm) return PKV_ERR_NULL;
+  auto it = bm->seqs.find(seq);
+  if (it == bm->seqs.end()) return PKV_ERR_STATE;
+  if (start < 0 || count < 0 || start + count > it->second.len) return PKV_ERR_ARG;
+  if (count > 0 && !slot_mapping) return PKV_ERR_NULL;
+  const auto& table = it->second.table;
+  for (int64_t i = 0; i < count; ++i) {
+    const int64_t t = start + i;
+    slot_mapping[i] = (int64_t)table[(size_t)(t / bm->width)] * bm->width + t % bm->width;
+  }
+  return PKV_OK;
+}
+
 int64_t pkv_bm_num_free(const pkv_block_manager* bm) {
   return bm ? (int64_t)bm->free_list.size() : -1;
 }

@@ -45,6 +45,16 @@ CONFIGS = {
         groups=16, forks=8, prompt=1031, slack=0.10,
         about="parallel sampling: 16 groups x 8 forks sharing a 1031-token prompt "
               "(last block partial), GQA 32/8, head_dim 128, bf16, block 16"),
+    "prefill": dict(
+        index=5, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
+        batch=8, prefix=0, chunk=2048, slack=0.10,
+        about="paged prefill: 8 prompts of 2048 tokens (no cached prefix), GQA 32/8, "
+              "head_dim 128, bf16, block 16, causal"),
+    "chunked": dict(
+        index=6, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
+        batch=8, prefix=4096, chunk=512, slack=0.10,
+        about="chunked prefill: 8 sequences with 4096 cached positions and a 512-token "
+              "chunk, GQA 32/8, head_dim 128, bf16, block 16, causal"),
     "long": dict(
         index=4, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
         batch=8, len_lo=16384, len_hi=32768, slack=0.10, partition_size=512,

@@ -139,3 +139,19 @@ def test_bad_arguments():
         bm.release(9)
     with pytest.raises(RuntimeError):
         bm.tables([0], 0)
+
+
+def test_slots_query_matches_oracle_translation():
+    rng = random.Random(9)
+    order = rng.sample(range(64), 64)
+    bm = BlockManager(64, 8, order)
+    pool = B.BlockPool(64, 8, free_order=order)
+    for s, n in enumerate([13, 1, 40, 8]):
+        bm.admit(s, n)
+        pool.admit(s, list(range(n)))
+        table = pool.table(s)
+        expect = [P.translate(t, 8, table)[3] for t in range(n)]
+        assert list(bm.slots(s, 0, n)) == expect
+        assert list(bm.slots(s, n // 2, n - n // 2)) == expect[n // 2:]
+    with pytest.raises(RuntimeError):
+        bm.slots(0, 10, 4)   # past the sequence end

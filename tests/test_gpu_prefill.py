@@ -1,0 +1,155 @@
+"""GPU paged prefill (causal chunk attention) against the oracle: geometry
+grid with cached prefixes and ragged chunks, the full chunked-prefill flow
+(block manager -> KV write -> prefill), agreement with decode for one-query
+chunks, stale NaN slots and invalid inputs."""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_145_gb300 as pkv
+from oracle import attention as A
+from oracle import blocks as B
+from paged_kv_cache_145_gb300 import synth
+from tests.workload import TOL, edge_tol, gpu_out_f64
+
+pytestmark = pytest.mark.gpu
+TORCH = synth.TORCH_DTYPE
+
+
+class PCase:
+    """Scattered tables over a random pool; per sequence a cached prefix and a
+    chunk of new queries (their keys already in the pool)."""
+
+    def __init__(self, dtype, H, Hk, D, b, prefix, chunk, seed=0, spare=3):
+        rng = np.random.default_rng(seed)
+        self.dtype, self.H, self.Hk, self.D, self.b = dtype, H, Hk, D, b
+        self.lens = [p_ + c for p_, c in zip(prefix, chunk)]
+        self.chunk = list(chunk)
+        self.starts = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+        nblk = [-(-L // b) for L in self.lens]
+        self.N = sum(nblk) + spare
+        perm = rng.permutation(self.N)
+        self.tables = np.full((len(self.lens), max(nblk) + 1), -1, dtype=np.int32)
+        pos = 0
+        for i, k in enumerate(nblk):
+            self.tables[i, :k] = perm[pos:pos + k]
+            pos += k
+        g = torch.Generator().manual_seed(seed)
+        self.k = torch.randn(self.N, Hk, b, D, generator=g).to(TORCH[dtype])
+        self.v = torch.randn(self.N, Hk, b, D, generator=g).to(TORCH[dtype])
+        self.q = torch.randn(int(self.starts[-1]), H, D, generator=g).to(TORCH[dtype])
+        self.scale = 1.0 / np.sqrt(D)
+
+    def gpu(self, lens=None, tables=None, starts=None, max_queries=None):
+        cache = pkv.PagedKVCache(self.k.cuda().clone(), self.v.cuda().clone())
+        out = pkv.paged_attention_prefill(
+            cache, self.q.cuda(), torch.from_numpy(self.starts if starts is None else starts).cuda(),
+            torch.from_numpy(self.tables if tables is None else tables).cuda(),
+            torch.tensor(self.lens if lens is None else lens, dtype=torch.int32).cuda(), self.scale,
+            max(self.chunk) if max_queries is None else max_queries)
+        return out, pkv.paged_get_device_error()
+
+    def oracle(self, seqs=None):
+        dt = self.dtype
+        return A.prefill_attention(synth.storage_numpy(self.q, dt), synth.storage_numpy(self.k, dt),
+                                   synth.storage_numpy(self.v, dt), [list(r) for r in self.tables],
+                                   self.lens, self.starts, self.scale, self.b, dt, seqs=seqs)
+
+
+PREFIX = [0, 0, 5, 100, 0, 17, 64]
+CHUNK = [1, 37, 64, 3, 130, 70, 65]
+
+GRID = [(dt, D, b, G) for dt in ("f16", "bf16") for D in (64, 128) for b in (16,) for G in (1, 4)]
+GRID += [("bf16", 128, b, 4) for b in (8, 32, 64)] + [("f16", 128, 16, 2), ("bf16", 128, 16, 8),
+                                                       ("f16", 64, 8, 8)]
+
+
+@pytest.mark.parametrize("dt,D,b,G", GRID)
+def test_prefill_geometry_grid(dt, D, b, G):
+    c = PCase(dt, 2 * G, 2, D, b, PREFIX, CHUNK, seed=hash((dt, D, b, G)) % 997)
+    out, err = c.gpu()
+    assert err == 0
+    got, ref = gpu_out_f64(out), c.oracle()
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= edge_tol(dt, ref))
+
+
+def test_prefill_chunked_flow_through_block_manager():
+    # Prefix of 300 cached positions per sequence, then a 64-query chunk:
+    # the native block manager extends each table and names the chunk's
+    # slots; the chunk's keys/values are written, then attended.
+    dt, b, Hk, G, D = "bf16", 16, 8, 4, 128
+    prefix, chunk = [300, 211, 0], [64, 100, 129]
+    n = 80
+    order = synth.free_order(5, n)
+    bm = pkv.BlockManager(n, b, order)
+    pool = B.BlockPool(n, b, free_order=order, auto_verify=False)
+    slots, o_slots = [], []
+    for s, (p_, c) in enumerate(zip(prefix, chunk)):
+        bm.admit(s, p_ + c)
+        pool.admit(s, list(range(p_ + c)))
+        slots.append(bm.slots(s, p_, c))
+        tab = pool.table(s)
+        o_slots += [tab[t // b] * b + t % b for t in range(p_, p_ + c)]
+    slots = np.concatenate(slots)
+    assert list(slots) == o_slots
+    tables, lens = bm.tables(range(3), max(bm.num_seq_blocks(s) for s in range(3)))
+    g = torch.Generator().manual_seed(6)
+    kp = torch.randn(n, Hk, b, D, generator=g).bfloat16()
+    vp = torch.randn(n, Hk, b, D, generator=g).bfloat16()
+    kn = torch.randn(len(slots), Hk, D, generator=g).bfloat16()
+    vn = torch.randn(len(slots), Hk, D, generator=g).bfloat16()
+    q = torch.randn(len(slots), Hk * G, D, generator=g).bfloat16()
+    starts = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    cache = pkv.PagedKVCache(kp.cuda(), vp.cuda())
+    pkv.paged_kv_write(cache, kn.cuda(), vn.cuda(), torch.from_numpy(slots).cuda())
+    out = pkv.paged_attention_prefill(cache, q.cuda(), torch.from_numpy(starts).cuda(),
+                                      torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda(),
+                                      0.0884, max(chunk))
+    assert pkv.paged_get_device_error() == 0
+    ek, ev, _ = A.write_tokens(synth.storage_numpy(kp, dt), synth.storage_numpy(vp, dt),
+                               synth.storage_numpy(kn, dt), synth.storage_numpy(vn, dt), o_slots, b)
+    assert np.array_equal(synth.storage_numpy(cache.k_cache, dt), ek)
+    ref = A.prefill_attention(synth.storage_numpy(q, dt), ek, ev, [pool.table(s) for s in range(3)],
+                              [p_ + c for p_, c in zip(prefix, chunk)], starts, 0.0884, b, dt)
+    assert np.max(np.abs(gpu_out_f64(out) - ref)) <= TOL[dt]
+
+
+def test_one_query_chunks_agree_with_decode():
+    c = PCase("bf16", 32, 8, 128, 16, [10, 500, 77, 1023], [1, 1, 1, 1], seed=4)
+    out, err = c.gpu()
+    assert err == 0
+    cache = pkv.PagedKVCache(c.k.cuda(), c.v.cuda())
+    dec = pkv.paged_attention_decode(cache, c.q.cuda(), torch.from_numpy(c.tables).cuda(),
+                                     torch.tensor(c.lens, dtype=torch.int32).cuda(), c.scale)
+    assert np.max(np.abs(gpu_out_f64(out) - gpu_out_f64(dec))) <= TOL["bf16"]
+
+
+@pytest.mark.parametrize("b", [8, 16, 64])
+def test_prefill_stale_nan_slots(b):
+    c = PCase("f16", 8, 2, 128, b, [3, 0, 40], [5, 17, 9], seed=7)
+    for s_, L in enumerate(c.lens):
+        last = int(c.tables[s_, (L - 1) // b])
+        c.k[last, :, (L - 1) % b + 1:] = float("nan")
+        c.v[last, :, (L - 1) % b + 1:] = float("nan")
+    out, err = c.gpu()
+    assert err == 0
+    got, ref = gpu_out_f64(out), c.oracle()
+    assert np.all(np.isfinite(got)) and np.all(np.abs(got - ref) <= edge_tol("f16", ref))
+
+
+def test_prefill_invalid_inputs_zero_rows():
+    c = PCase("bf16", 8, 2, 64, 16, [10, 10, 10], [4, 4, 4], seed=8)
+    lens = [14, 3, 14]             # sequence 1: chunk longer than the sequence
+    tables = c.tables.copy()
+    tables[2, 0] = c.N + 4         # sequence 2: table entry outside the pool
+    out, err = c.gpu(lens=lens, tables=tables)
+    assert err == (pkv.PKV_DEV_SEQ_LEN | pkv.PKV_DEV_TABLE_RANGE)
+    got = gpu_out_f64(out)
+    assert np.all(got[4:12] == 0)
+    ref = c.oracle(seqs=[0])
+    assert np.max(np.abs(got[:4] - ref[:4])) <= edge_tol("bf16", ref[:4]).max()
+    # A chunk longer than the declared bound is refused on the device too.
+    out, err = c.gpu(max_queries=3)
+    assert err == pkv.PKV_DEV_SEQ_LEN and np.all(gpu_out_f64(out) == 0)
