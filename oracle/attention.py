@@ -29,12 +29,53 @@ import math
 
 import numpy as np
 
-DTYPES = ("f32", "f16", "bf16")
+DTYPES = ("f32", "f16", "bf16", "e4m3")
+
+
+# ---------------------------------------------------------------------------
+# FP8 E4M3 (OCP 8-bit floating point, "E4M3" variant): 1 sign bit, 4 exponent
+# bits with bias 7, 3 mantissa bits; exponent 0 encodes subnormals
+# (mantissa / 8 * 2^-6); the all-ones exponent with all-ones mantissa is NaN;
+# there are no infinities, so the largest finite magnitude is 1.75 * 2^8 =
+# 448.  Cache codes here are produced with round-to-nearest-even and
+# saturation to +-448 ("satfinite").
+# ---------------------------------------------------------------------------
+def e4m3_decode(codes):
+    """Codes (uint8) to float64 values; NaN for the two NaN codes."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    exp = (c >> 3) & 0xF
+    man = (c & 7).astype(np.float64)
+    val = np.where(exp == 0, man / 8.0 * 2.0 ** -6, (1.0 + man / 8.0) * 2.0 ** (exp - 7.0))
+    val = np.where((exp == 15) & ((c & 7) == 7), np.nan, val)
+    return sign * val
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F))  # codes 0x00..0x7E: 0 .. 448, increasing
+
+
+def e4m3_encode(x):
+    """float32 values to E4M3 codes: nearest value, ties to the even code
+    (even mantissa), magnitudes beyond 448 saturate to 448, NaN to 0x7F."""
+    x = np.asarray(x, dtype=np.float32).astype(np.float64)
+    mag = np.abs(x)
+    hi = np.clip(np.searchsorted(_E4M3_POS, mag, side="left"), 0, 0x7E)
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_hi = np.abs(_E4M3_POS[hi] - mag)
+    d_lo = np.abs(mag - _E4M3_POS[lo])
+    pick = np.where(d_lo < d_hi, lo, np.where(d_hi < d_lo, hi, np.where(lo % 2 == 0, lo, hi)))
+    pick = np.where(mag >= 448.0, 0x7E, pick)
+    code = (pick | np.where(np.signbit(x), 0x80, 0)).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
 
 
 def to_f64(x, dtype):
     """Widen stored elements to float64 exactly."""
     x = np.asarray(x)
+    if dtype == "f64":
+        return x.astype(np.float64)
+    if dtype == "e4m3":
+        return e4m3_decode(x)
     if dtype == "f32":
         return x.astype(np.float32, copy=False).astype(np.float64)
     if dtype == "f16":
@@ -81,6 +122,29 @@ def write_tokens(k_pool, v_pool, k_new, v_new, slot_mapping, b):
             k_out[blk, h, off, :] = k_new[i, h, :]
             v_out[blk, h, off, :] = v_new[i, h, :]
     return k_out, v_out, bad
+
+
+def write_tokens_fp8(k_pool, v_pool, k_new, v_new, slot_mapping, b, k_scale, v_scale, io_dtype):
+    """KV write into an FP8 E4M3 pool with one scale per KV head.
+
+    Like :func:`write_tokens`, but each new element x (stored in
+    ``io_dtype``, widened exactly to float32) is stored as the code
+    ``e4m3(x / scale[h])``, the division done in float32 (correctly
+    rounded).  Reading the cache back gives ``value(code) * scale[h]``.
+    """
+    kq = np.empty(k_new.shape, dtype=np.uint8)
+    vq = np.empty(v_new.shape, dtype=np.uint8)
+    for h in range(k_new.shape[1]):
+        kx = to_f64(k_new[:, h], io_dtype).astype(np.float32)
+        vx = to_f64(v_new[:, h], io_dtype).astype(np.float32)
+        kq[:, h] = e4m3_encode(kx / np.float32(k_scale[h]))
+        vq[:, h] = e4m3_encode(vx / np.float32(v_scale[h]))
+    return write_tokens(k_pool, v_pool, kq, vq, slot_mapping, b)
+
+
+def dequantize_pool(codes, scales):
+    """float64 values of an E4M3 pool ``[N, Hk, b, D]`` with per-head scales."""
+    return e4m3_decode(codes) * np.asarray(scales, dtype=np.float64)[None, :, None, None]
 
 
 # ---------------------------------------------------------------------------
@@ -164,7 +228,8 @@ def _check_row(table, length, n_blocks, b, max_len):
     return all(0 <= int(x) < n_blocks for x in used)
 
 
-def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, max_len=None):
+def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, max_len=None,
+              q_dtype=None, k_scale=None, v_scale=None):
     """Single-query attention of every sequence over its paged keys/values.
 
     For sequence s and query head h (KV head ``h // (H // Hk)``, query heads
@@ -175,7 +240,9 @@ def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, m
         out[s, h] = sum_t exp(z_t - max z) V_t / sum_t exp(z_t - max z)
 
     ``q``: ``[S, H, D]``; pools ``[N, Hk, b, D]``; ``tables``: ``S`` lists
-    (or a 2-D array) of physical block ids; all stored in ``dtype``.  Rows
+    (or a 2-D array) of physical block ids; all stored in ``dtype``.  For an
+    FP8 (``"e4m3"``) pool, ``q`` is stored in ``q_dtype`` and key/value rows
+    of KV head h are ``value(code) * k_scale[h]`` / ``* v_scale[h]``.  Rows
     whose length or table entries are invalid are set to zero and their
     sequence index is reported.  ``seqs`` restricts the work to a subset of
     sequences (other rows are NaN).  ``max_len`` is the caller's bound on
@@ -202,8 +269,12 @@ def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, m
         for kvh in range(kv_heads):
             keys = to_f64(gather_rows(k_pool, table, length, b, kvh), dtype)
             vals = to_f64(gather_rows(v_pool, table, length, b, kvh), dtype)
+            if k_scale is not None:
+                keys = keys * float(k_scale[kvh])
+            if v_scale is not None:
+                vals = vals * float(v_scale[kvh])
             for h in range(kvh * group, (kvh + 1) * group):
-                z = scale * (keys @ to_f64(q[s, h], dtype))
+                z = scale * (keys @ to_f64(q[s, h], q_dtype or dtype))
                 w = np.exp(z - z.max())
                 out[s, h] = (w @ vals) / w.sum()
     return out, bad

@@ -484,3 +484,48 @@ def check_prefill(prefill_attention, attention, seed=11):
     out2 = prefill_attention(q, k2, v2, tables, lens, starts, 0.35, b, "f32", seqs=[0])
     assert np.array_equal(out2[starts[0]:starts[0] + 2], out[starts[0]:starts[0] + 2])
     assert not np.allclose(out2[starts[0] + 2], out[starts[0] + 2])
+
+
+def check_e4m3(e4m3_encode, e4m3_decode, seed=12):
+    """E4M3 codes: torch's float8_e4m3fn cast (round to nearest even) on
+    in-range values, the format's landmark codes, saturation, and the
+    half-step error bound."""
+    rng = np.random.default_rng(seed)
+    x = np.concatenate([rng.standard_normal(4000) * 40, rng.uniform(-464, 464, 4000),
+                        [0.0, 1.0, 448.0, -448.0, 2.0 ** -9, 1.0625, 1.1875, 464.0, 0.5, 240.0]])
+    x = x.astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(e4m3_encode(x), ref)
+    # landmarks from the format: 1.0, the largest finite, the smallest subnormal
+    assert e4m3_encode(np.float32(1.0)) == 0x38 and e4m3_decode(0x38) == 1.0
+    assert e4m3_decode(0x7E) == 448.0 and e4m3_decode(0x01) == 2.0 ** -9
+    assert np.isnan(e4m3_decode(0x7F)) and np.isnan(e4m3_decode(0xFF))
+    # saturation instead of NaN beyond the largest finite
+    assert e4m3_encode(np.float32(1e4)) == 0x7E and e4m3_encode(np.float32(-1e4)) == 0xFE
+    # round trip within half a step (3 mantissa bits: relative 2^-4)
+    y = np.abs(rng.uniform(2.0 ** -6, 448, 2000).astype(np.float32))
+    assert np.all(np.abs(e4m3_decode(e4m3_encode(y)) - y) <= y * 2.0 ** -4)
+
+
+def check_fp8_write_and_attention(write_tokens_fp8, dequantize_pool, attention, e4m3_encode):
+    rng = np.random.default_rng(13)
+    n, hk, b, d = 6, 2, 4, 8
+    kp = rng.integers(0, 0x7E, size=(n, hk, b, d)).astype(np.uint8)
+    vp = rng.integers(0, 0x7E, size=(n, hk, b, d)).astype(np.uint8)
+    kn = rng.standard_normal((3, hk, d)).astype(np.float16)
+    vn = rng.standard_normal((3, hk, d)).astype(np.float16)
+    ks, vs = np.array([0.02, 0.5], np.float32), np.array([0.01, 0.25], np.float32)
+    slots = [5, 17, 22]
+    k2, v2, bad = write_tokens_fp8(kp, vp, kn, vn, slots, b, ks, vs, "f16")
+    assert bad == []
+    for i, sl in enumerate(slots):
+        for h in range(hk):
+            assert np.array_equal(k2[sl // b, h, sl % b],
+                                  e4m3_encode(kn[i, h].astype(np.float32) / ks[h]))
+    # Attention over an FP8 pool equals attention over its dequantized values.
+    q = rng.standard_normal((2, hk * 2, d)).astype(np.float16)
+    tables, lens = [[3, 1], [0, 5, 2]], [7, 10]
+    out, _ = attention(q, k2, v2, tables, lens, 0.3, b, "e4m3", q_dtype="f16", k_scale=ks, v_scale=vs)
+    ref, _ = attention(q.astype(np.float64), dequantize_pool(k2, ks), dequantize_pool(v2, vs), tables,
+                       lens, 0.3, b, "f64")
+    assert np.max(np.abs(out - ref)) < 1e-12

@@ -90,3 +90,12 @@ def test_swap():
 
 def test_prefill():
     pins.check_prefill(A.prefill_attention, A.attention)
+
+
+def test_e4m3():
+    pins.check_e4m3(A.e4m3_encode, A.e4m3_decode)
+
+
+def test_fp8_write_and_attention():
+    pins.check_fp8_write_and_attention(A.write_tokens_fp8, A.dequantize_pool, A.attention,
+                                       A.e4m3_encode)

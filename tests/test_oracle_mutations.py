@@ -121,3 +121,13 @@ def test_prefill_off_by_one_position():
     bad = mutant(A.prefill_attention, "visible = first + i + 1", "visible = first + i")
     with pytest.raises((AssertionError, IndexError, ValueError)):
         pins.check_prefill(bad, A.attention)
+
+
+def test_e4m3_ties_away_from_even():
+    bad = mutant(A.e4m3_encode, "np.where(lo % 2 == 0, lo, hi)", "hi")
+    fails(pins.check_e4m3, bad, A.e4m3_decode)
+
+
+def test_e4m3_wrong_bias():
+    bad = mutant(A.e4m3_decode, "2.0 ** (exp - 7.0)", "2.0 ** (exp - 8.0)")
+    fails(pins.check_e4m3, A.e4m3_encode, bad)
