@@ -44,17 +44,23 @@ from paged_kv_cache_145_gb300 import synth  # noqa: E402
 METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
 
 # DRAM bytes (read + write) per launch of the decode kernels, from ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, with the
-# hash of the kernel sources they were taken on.  A stale hash reports null.
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and KV
+# dtype, with the hash of the kernel sources they were taken on.  A stale
+# hash reports null.
 TRAFFIC = {
-    "opt13b": (1280290784, "29e456e9784abf13"),
-    "gqa": (1128956920, "29e456e9784abf13"),
+    "opt13b": (1280275968, "efd6c816a71e6062"),
+    "gqa": (1128982784, "efd6c816a71e6062"),
+    "opt13b/fp8": (645104896, "efd6c816a71e6062"),
+    "gqa/fp8": (568320256, "efd6c816a71e6062"),
 }
+
+KERNEL_SOURCES = ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_mma_fp8.cuh",
+                  "decode_launch.cuh")
 
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for f in ("decode.cuh", "common.cuh"):
+    for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, "paged_kv_cache_145_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -81,7 +87,7 @@ class Workload:
     isolates the cost of scattered pages from the rest of the paging.
     """
 
-    def __init__(self, name, rank=0, block_size=None, table="shuffled"):
+    def __init__(self, name, rank=0, block_size=None, table="shuffled", kv_dtype=None):
         import paged_kv_cache_145_gb300 as pkv
 
         cfg = synth.CONFIGS[name]
@@ -89,7 +95,9 @@ class Workload:
         self.b = b = block_size or cfg["block_size"]
         self.table_kind = table
         self.H, self.Hk, self.D, self.dtype = cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
-        self.elt = synth.ELEM_BYTES[self.dtype]
+        self.elt = synth.ELEM_BYTES[self.dtype]                # q, out, new k/v
+        self.kv_dtype = kv_dtype or self.dtype
+        self.kv_elt = synth.ELEM_BYTES[self.kv_dtype]          # cache elements
         ceil_div = lambda a, c: -(-a // c)  # noqa: E731
         if name == "fork":
             g, f, prompt = cfg["groups"], cfg["forks"], cfg["prompt"]
@@ -123,7 +131,7 @@ class Workload:
     # Algorithmic bytes, counted without reuse across sequences.
     def decode_bytes(self, part):
         L = self.seq_lens.astype(np.int64)
-        kv = 2 * L * self.Hk * self.D * self.elt
+        kv = 2 * L * self.Hk * self.D * self.kv_elt
         qo = 2 * self.H * self.D * self.elt
         table = 4 * (-(-L // self.b)) + 4
         nparts = -(-L // part)
@@ -132,10 +140,10 @@ class Workload:
 
     def write_bytes(self):
         n = self.S
-        return 2 * 2 * n * self.Hk * self.D * self.elt + 8 * n
+        return 2 * n * self.Hk * self.D * (self.elt + self.kv_elt) + 8 * n
 
     def copy_bytes(self):
-        return 2 * 2 * len(self.pairs) * self.Hk * self.b * self.D * self.elt + 16 * len(self.pairs)
+        return 2 * 2 * len(self.pairs) * self.Hk * self.b * self.D * self.kv_elt + 16 * len(self.pairs)
 
 
 # ---------------------------------------------------------------------------
@@ -339,12 +347,22 @@ def run_ours(args):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = oracle_timed(args.config, args.cpu_budget)
 
-    w = Workload(args.config, rank=rank, block_size=args.block_size or None, table=args.table)
+    kv_dtype = "e4m3" if args.kv_dtype == "fp8" else None
+    w = Workload(args.config, rank=rank, block_size=args.block_size or None, table=args.table,
+                 kv_dtype=kv_dtype)
     dt = synth.TORCH_DTYPE[w.dtype]
     seed = synth.seed_of(args.config, 3) + 10 * rank
     shape = (w.N, w.Hk, w.b, w.D)
-    cache = pkv.PagedKVCache(synth.normal(seed, shape, w.dtype, device="cuda"),
-                             synth.normal(seed + 1, shape, w.dtype, device="cuda"))
+    if kv_dtype:
+        # FP8 E4M3 pool with one scale per KV head (1/64: N(0, 1) values
+        # within +-4 land inside the format's +-448 range).
+        scale = torch.full((w.Hk,), 1.0 / 64, dtype=torch.float32, device=dev)
+        cache = pkv.PagedKVCache(synth.random_codes(seed, shape, device="cuda"),
+                                 synth.random_codes(seed + 1, shape, device="cuda"),
+                                 scale, scale.clone(), dt)
+    else:
+        cache = pkv.PagedKVCache(synth.normal(seed, shape, w.dtype, device="cuda"),
+                                 synth.normal(seed + 1, shape, w.dtype, device="cuda"))
     q_h = synth.normal(seed + 2, (w.S, w.H, w.D), w.dtype).pin_memory()
     k_h = synth.normal(seed + 3, (w.S, w.Hk, w.D), w.dtype).pin_memory()
     v_h = synth.normal(seed + 4, (w.S, w.Hk, w.D), w.dtype).pin_memory()
@@ -356,9 +374,8 @@ def run_ours(args):
     slots, tables, lens, pairs = slots_h.to(dev), tables_h.to(dev), lens_h.to(dev), pairs_h.to(dev)
     out = torch.empty_like(q)
     out_h = torch.empty_like(q_h).pin_memory()
-    cref = pkv.PagedKVCache(cache.k_cache, cache.v_cache)
-    part = pkv.paged_attention_partition_size(cref, w.S, w.H, w.max_len, args.partition)
-    ws_bytes = pkv.paged_attention_workspace_bytes(cref, w.S, w.H, w.max_len, part)
+    part = pkv.paged_attention_partition_size(cache, w.S, w.H, w.max_len, args.partition)
+    ws_bytes = pkv.paged_attention_workspace_bytes(cache, w.S, w.H, w.max_len, part)
     ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
     scale = 1.0 / math.sqrt(w.D)
     has_pairs = len(w.pairs) > 0
@@ -438,7 +455,8 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     achieved = dec_bytes / (decode_ms / 1e3) / 1e9
     src_hash = kernel_source_hash()
-    tr = TRAFFIC.get(args.config)
+    default_shape = args.partition == 0 and args.block_size == 0 and args.table == "shuffled"
+    tr = TRAFFIC.get(args.config + ("/fp8" if kv_dtype else "")) if default_shape else None
     traffic = tr[0] if tr and tr[1] == src_hash else None
     line = {
         "metric": METRIC,
@@ -451,9 +469,10 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": w.dtype if not kv_dtype else "%s (KV cache e4m3)" % w.dtype,
         "data": "synthetic",
         "config": {"workload": args.config, "about": w.cfg["about"], "num_seqs": w.S,
+                   "kv_dtype": w.kv_dtype,
                    "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
                    "pool_blocks": w.N, "partition_size": part, "table": w.table_kind,
                    "slot_utilization": round(w.utilization, 5),
@@ -690,6 +709,9 @@ def main():
     ap.add_argument("--config", default="opt13b", choices=sorted(k for k in synth.CONFIGS if k != "tiny"))
     ap.add_argument("--partition", type=int, default=0, help="positions per partition (0 = default)")
     ap.add_argument("--block-size", type=int, default=0, help="override the workload's block size")
+    ap.add_argument("--kv-dtype", choices=("native", "fp8"), default="native",
+                    help="cache element type: the workload's own (default) or FP8 E4M3 with "
+                         "per-head scales")
     ap.add_argument("--table", choices=("shuffled", "identity"), default="shuffled",
                     help="physical block order: shuffled pool (default) or consecutive blocks")
     ap.add_argument("--op", choices=("step", "write", "copy", "swap", "prefill"), default="step",

@@ -52,8 +52,12 @@
 extern "C" {
 #endif
 
-/* Element type of q, the caches and out (one type for all of them). */
-typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 } pkv_dtype;
+/* Element type of the caches.  For PKV_F32 / PKV_F16 / PKV_BF16 pools, q,
+ * out and the new keys/values have the same type.  PKV_FP8_E4M3 pools hold
+ * 8-bit E4M3 codes (OCP FP8: bias 7, 3 mantissa bits, largest finite 448)
+ * with one float scale per KV head for keys and one for values; q, out and
+ * the new keys/values are then 16-bit (pkv_cache.io_dtype). */
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dtype;
 
 /* Host-side return codes. */
 #define PKV_OK              0
@@ -84,6 +88,10 @@ typedef struct {
   int32_t num_kv_heads;  /* Hk                                               */
   int32_t head_dim;      /* D                                                */
   int32_t dtype;         /* a pkv_dtype                                      */
+  /* FP8 pools only (ignored otherwise): */
+  const float* k_scale;  /* device float[Hk]: key of head h = value(code) * k_scale[h] */
+  const float* v_scale;  /* device float[Hk]: likewise for values            */
+  int32_t io_dtype;      /* PKV_F16 or PKV_BF16: type of q, out, new k/v     */
 } pkv_cache;
 
 /*
@@ -96,13 +104,16 @@ typedef struct {
  * [0, num_tokens) with slot = slot_mapping[i] >= 0:
  *     k_cache[slot / b][h][slot % b][:] = k[i][h][:]   for every KV head h
  *     v_cache[slot / b][h][slot % b][:] = v[i][h][:]
- * Elements are copied bit for bit.  A negative slot marks padding and is
+ * Elements are copied bit for bit.  For an FP8 pool the new elements (of
+ * io_dtype, widened to float32) are stored as e4m3(x / scale[h]) with the
+ * division in float32 (round to nearest), round-to-nearest-even and
+ * saturation to +-448.  A negative slot marks padding and is
  * skipped silently; a slot >= num_blocks * b is skipped and sets
  * PKV_DEV_SLOT_RANGE.  Two tokens with the same slot race (last writer
  * undefined).
  *
  *   k, v          device, [num_tokens][num_kv_heads][head_dim], contiguous,
- *                 cache dtype, 16-byte aligned
+ *                 cache dtype (io_dtype for FP8 pools), 16-byte aligned
  *   slot_mapping  device, int64[num_tokens]
  */
 int paged_kv_write(const pkv_cache* cache, const void* k, const void* v,
@@ -149,7 +160,9 @@ size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
  * and K_t, V_t the rows of position t found through the table:
  *     z_t = scale * dot(q[s][h], K_t)                    t = 0 .. L-1
  *     out[s][h] = sum_t e^(z_t - max z) V_t / sum_t e^(z_t - max z)
- * accumulated in float32 and rounded once to the output type.
+ * accumulated in float32 and rounded once to the output type.  For FP8
+ * pools K_t and V_t are the codes' values times the head's scales and q,
+ * out are io_dtype.
  *
  * Long sequences are split into partitions of `partition_size` positions
  * processed by separate thread blocks; a second kernel merges them
@@ -191,7 +204,8 @@ int paged_attention_decode(const pkv_cache* cache, const void* q,
  * chunk sits at position L - Q + i and attends to positions 0 .. L - Q + i:
  *     out[query_starts[s] + i][h] = softmax-weighted mean, as in
  *     paged_attention_decode, over the first L - Q + i + 1 positions
- * accumulated in float32 on tensor cores.  fp16 and bf16 pools only.
+ * accumulated in float32 on tensor cores.  fp16 and bf16 pools only (not
+ * FP8).
  *
  *   q, out        device, [total_queries][num_heads][head_dim], cache dtype
  *   query_starts  device, int32[num_seqs + 1], non-decreasing, last <=

@@ -21,7 +21,8 @@ from ._lib import (PKV_DEV_PAIR_RANGE, PKV_DEV_SEQ_LEN, PKV_DEV_SLOT_RANGE,  # n
                    PKV_DEV_TABLE_RANGE, PKV_DEV_TIMEOUT, PKV_ERR_NOMEM, PKV_SWAP_IN,
                    PKV_SWAP_OUT)
 
-_DTYPE_CODE = {torch.float32: _lib.PKV_F32, torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16}
+_DTYPE_CODE = {torch.float32: _lib.PKV_F32, torch.float16: _lib.PKV_F16, torch.bfloat16: _lib.PKV_BF16,
+               torch.float8_e4m3fn: _lib.PKV_FP8_E4M3}
 
 __all__ = [
     "PagedKVCache", "BlockManager", "paged_kv_write", "paged_attention_decode",
@@ -58,21 +59,42 @@ def _need(t, name, dtype=None, device=None):
 
 
 class PagedKVCache:
-    """The physical pool: two ``[N, Hk, b, D]`` tensors (keys, values)."""
+    """The physical pool: two ``[N, Hk, b, D]`` tensors (keys, values).
 
-    def __init__(self, k_cache, v_cache):
+    FP8 pools (``torch.float8_e4m3fn``) also take ``k_scale`` / ``v_scale``
+    (float32 CUDA tensors ``[Hk]``: a key of head h is its code's value times
+    ``k_scale[h]``) and ``io_dtype`` (float16 or bfloat16: the type of q, out
+    and the new keys/values).  For other pools ``io_dtype`` is the pool's.
+    """
+
+    def __init__(self, k_cache, v_cache, k_scale=None, v_scale=None, io_dtype=None):
         _need(k_cache, "k_cache")
         _need(v_cache, "v_cache", k_cache.dtype, k_cache.device)
         if k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
             raise ValueError("k_cache and v_cache must both be [N, Hk, b, D]")
         if k_cache.dtype not in _DTYPE_CODE:
-            raise ValueError("cache dtype must be float32, float16 or bfloat16")
+            raise ValueError("cache dtype must be float32, float16, bfloat16 or float8_e4m3fn")
         self.k_cache, self.v_cache = k_cache, v_cache
         self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim = k_cache.shape
         self.dtype, self.device = k_cache.dtype, k_cache.device
+        self.k_scale = self.v_scale = None
+        if self.dtype == torch.float8_e4m3fn:
+            if io_dtype not in (torch.float16, torch.bfloat16):
+                raise ValueError("an FP8 pool needs io_dtype float16 or bfloat16")
+            for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+                _need(t, name, torch.float32, self.device)
+                if t.shape != (self.num_kv_heads,):
+                    raise ValueError("%s must be [kv_heads]" % name)
+            self.k_scale, self.v_scale = k_scale, v_scale
+            self.io_dtype = io_dtype
+        else:
+            self.io_dtype = self.dtype
         self._c = _lib.pkv_cache(k_cache.data_ptr(), v_cache.data_ptr(), self.num_blocks,
                                  self.block_size, self.num_kv_heads, self.head_dim,
-                                 _DTYPE_CODE[self.dtype])
+                                 _DTYPE_CODE[self.dtype],
+                                 self.k_scale.data_ptr() if self.k_scale is not None else None,
+                                 self.v_scale.data_ptr() if self.v_scale is not None else None,
+                                 _DTYPE_CODE[self.io_dtype])
 
     @classmethod
     def empty(cls, num_blocks, block_size, num_kv_heads, head_dim, dtype, device="cuda"):
@@ -87,8 +109,8 @@ class PagedKVCache:
 
 def paged_kv_write(cache, k, v, slot_mapping, stream=None):
     """Store ``k``/``v`` ``[T, Hk, D]`` at ``slot_mapping`` (int64 ``[T]``)."""
-    _need(k, "k", cache.dtype, cache.device)
-    _need(v, "v", cache.dtype, cache.device)
+    _need(k, "k", cache.io_dtype, cache.device)
+    _need(v, "v", cache.io_dtype, cache.device)
     _need(slot_mapping, "slot_mapping", torch.int64, cache.device)
     n = slot_mapping.numel()
     if k.shape != (n, cache.num_kv_heads, cache.head_dim) or v.shape != k.shape:
@@ -119,7 +141,7 @@ def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, ma
     size).  Allocates ``out`` and the split-K workspace when not given.
     Returns ``out``.
     """
-    _need(q, "q", cache.dtype, cache.device)
+    _need(q, "q", cache.io_dtype, cache.device)
     _need(block_tables, "block_tables", torch.int32, cache.device)
     _need(seq_lens, "seq_lens", torch.int32, cache.device)
     if q.dim() != 3 or q.shape[2] != cache.head_dim:
@@ -129,7 +151,7 @@ def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, ma
         raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", cache.dtype, cache.device)
+    _need(out, "out", cache.io_dtype, cache.device)
     if out.shape != q.shape:
         raise ValueError("out must have q's shape")
     bound = max_seq_len if max_seq_len else block_tables.shape[1] * cache.block_size
@@ -154,7 +176,7 @@ def paged_attention_prefill(cache, q, query_starts, block_tables, seq_lens, scal
     (positions including the chunk); ``max_queries``: host bound on any
     chunk's length.  Returns ``out``.
     """
-    _need(q, "q", cache.dtype, cache.device)
+    _need(q, "q", cache.io_dtype, cache.device)
     _need(query_starts, "query_starts", torch.int32, cache.device)
     _need(block_tables, "block_tables", torch.int32, cache.device)
     _need(seq_lens, "seq_lens", torch.int32, cache.device)
@@ -166,7 +188,7 @@ def paged_attention_prefill(cache, q, query_starts, block_tables, seq_lens, scal
         raise ValueError("query_starts must be [S + 1] and block_tables [S, max_blocks]")
     if out is None:
         out = torch.empty_like(q)
-    _need(out, "out", cache.dtype, cache.device)
+    _need(out, "out", cache.io_dtype, cache.device)
     _lib.check(_lib.lib().paged_attention_prefill(
         cache.ref, _ptr(q), q.shape[0], _ptr(query_starts), num_seqs, int(max_queries),
         _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), q.shape[1], float(scale),

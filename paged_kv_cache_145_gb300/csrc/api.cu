@@ -12,6 +12,11 @@
 
 int pkv_launch_kv_write(const pkv_cache* c, const void* k, const void* v, const int64_t* slots,
                         int64_t num_tokens, size_t elem_bytes, cudaStream_t stream);
+int pkv_launch_kv_write_fp8(const pkv_cache* c, const void* k, const void* v,
+                            const int64_t* slots, int64_t num_tokens, cudaStream_t stream);
+int pkv_launch_decode_fp8(const pkv::DecodeParams& p, int num_seqs, int head_dim, int block_size,
+                          int group, int io_dtype, const pkv::DecodeMaps* maps, bool mma,
+                          cudaStream_t stream);
 int pkv_launch_block_copy(const pkv_cache* c, const int64_t* pairs, int64_t num_pairs,
                           size_t elem_bytes, cudaStream_t stream);
 int pkv_launch_block_swap(const pkv_cache* c, void* host_k, void* host_v, int64_t host_blocks,
@@ -44,8 +49,20 @@ size_t elem_bytes(int dtype) {
     case PKV_F32: return 4;
     case PKV_F16: return 2;
     case PKV_BF16: return 2;
+    case PKV_FP8_E4M3: return 1;
   }
   return 0;
+}
+
+// Pools whose elements the kernels must interpret (write, attention): an
+// FP8 pool needs both scale arrays and a 16-bit io type.
+int check_scales(const pkv_cache* c) {
+  if (c->dtype != PKV_FP8_E4M3) return PKV_OK;
+  if (c->io_dtype != PKV_F16 && c->io_dtype != PKV_BF16) return PKV_ERR_ARG;
+  if (!c->k_scale || !c->v_scale) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(c->k_scale) & 3u) || (reinterpret_cast<uintptr_t>(c->v_scale) & 3u))
+    return PKV_ERR_ALIGN;
+  return PKV_OK;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -106,13 +123,18 @@ WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_len
   return w;
 }
 
-// The tensor-core decode kernel serves fp16 / bf16 pools whose query heads
-// come in groups of 2, 4 or 8 (any supported block size).  PKV_DECODE_KERNEL=simt in the environment selects the
-// CUDA-core kernel instead (read on every call).
-bool use_mma(const pkv_cache* c, int group) {
-  if (c->dtype == PKV_F32 || group < 2) return false;
+// The tensor-core decode kernels serve fp16 / bf16 pools whose query heads
+// come in groups of 2, 4 or 8, and every FP8 pool.  PKV_DECODE_KERNEL=simt in
+// the environment selects the CUDA-core kernel instead (read on every call).
+bool simt_forced() {
   const char* env = std::getenv("PKV_DECODE_KERNEL");
-  return !(env && std::strcmp(env, "simt") == 0);
+  return env && std::strcmp(env, "simt") == 0;
+}
+
+bool use_mma(const pkv_cache* c, int group) {
+  if (c->dtype == PKV_FP8_E4M3) return !simt_forced();  // every grouping
+  if (c->dtype == PKV_F32 || group < 2) return false;
+  return !simt_forced();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -129,8 +151,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Describes a [N][Hk][b][D] pool as a 4-D tensor (D fastest) read in boxes of
-// min(b, 16) rows x 64 elements (128 bytes) with the 128-byte shared-memory
-// swizzle.
+// min(b, 16) rows x 128 bytes (64 16-bit elements, or 128 FP8 codes) with the
+// 128-byte shared-memory swizzle.
 bool encode_pool_map(CUtensorMap* map, const pkv_cache* c, void* base) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
@@ -139,10 +161,13 @@ bool encode_pool_map(CUtensorMap* map, const pkv_cache* c, void* base) {
                               (cuuint64_t)c->num_kv_heads, (cuuint64_t)c->num_blocks};
   const cuuint64_t strides[3] = {c->head_dim * elt, c->block_size * c->head_dim * elt,
                                  (cuuint64_t)c->num_kv_heads * c->block_size * c->head_dim * elt};
-  const cuuint32_t box[4] = {64, (cuuint32_t)(c->block_size < 16 ? c->block_size : 16), 1, 1};
+  const cuuint32_t box[4] = {(cuuint32_t)(128 / elt),
+                             (cuuint32_t)(c->block_size < 16 ? c->block_size : 16), 1, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType ty =
-      c->dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+      c->dtype == PKV_FP8_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+      : c->dtype == PKV_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                               : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
   return enc(map, ty, 4, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -168,12 +193,16 @@ int paged_kv_write(const pkv_cache* cache, const void* k, const void* v,
                    const int64_t* slot_mapping, int64_t num_tokens, cudaStream_t stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
+  rc = check_scales(cache);
+  if (rc) return rc;
   if (num_tokens < 0 || num_tokens > INT32_MAX) return PKV_ERR_ARG;
   if (num_tokens == 0) return PKV_OK;
   if (!k || !v || !slot_mapping) return PKV_ERR_NULL;
   if (!aligned16(k) || !aligned16(v) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return PKV_ERR_ALIGN;
   if (!pkv_error_word()) return PKV_ERR_CUDA;
+  if (cache->dtype == PKV_FP8_E4M3)
+    return pkv_launch_kv_write_fp8(cache, k, v, slot_mapping, num_tokens, stream);
   return pkv_launch_kv_write(cache, k, v, slot_mapping, num_tokens, elem_bytes(cache->dtype),
                              stream);
 }
@@ -201,6 +230,8 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
                            void* workspace, size_t workspace_bytes, int32_t partition_size,
                            cudaStream_t stream) {
   int rc = check_cache(cache);
+  if (rc) return rc;
+  rc = check_scales(cache);
   if (rc) return rc;
   if (num_seqs < 0 || num_seqs > 65535 || max_blocks_per_seq < 1 || num_heads < 1)
     return PKV_ERR_ARG;
@@ -244,7 +275,22 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
   p.ws_o = ws.total ? reinterpret_cast<float*>(static_cast<char*>(workspace) + ws.o_offset)
                     : nullptr;
   p.err = err;
+  p.k_scale = cache->k_scale;
+  p.v_scale = cache->v_scale;
   const int group = num_heads / cache->num_kv_heads;
+  if (cache->dtype == PKV_FP8_E4M3) {
+    const bool mma = use_mma(cache, group);
+    pkv::DecodeMaps fmaps;
+    const pkv::DecodeMaps* fmp = nullptr;
+    if (mma && cache->head_dim == 128) {  // direct key fragments read TMA-swizzled codes
+      if (!encode_pool_map(&fmaps.k, cache, cache->k_cache) ||
+          !encode_pool_map(&fmaps.v, cache, cache->v_cache))
+        return PKV_ERR_CUDA;
+      fmp = &fmaps;
+    }
+    return pkv_launch_decode_fp8(p, num_seqs, cache->head_dim, cache->block_size, group,
+                                 cache->io_dtype, fmp, mma, stream);
+  }
   pkv::DecodeMaps maps;
   const pkv::DecodeMaps* mp = nullptr;
   if (use_mma(cache, group)) {
@@ -274,7 +320,9 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
     return PKV_ERR_ARG;
   if (num_seqs == 0 || total_queries == 0) return PKV_OK;
   if (!q || !out || !query_starts || !block_tables || !seq_lens) return PKV_ERR_NULL;
-  if (cache->dtype == PKV_F32 || !decode_geometry_ok(cache, num_heads)) return PKV_ERR_GEOMETRY;
+  if (cache->dtype == PKV_F32 || cache->dtype == PKV_FP8_E4M3 ||
+      !decode_geometry_ok(cache, num_heads))
+    return PKV_ERR_GEOMETRY;
   if (cache->num_kv_heads > 65535 || (int64_t)max_blocks_per_seq * cache->block_size > INT32_MAX)
     return PKV_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||

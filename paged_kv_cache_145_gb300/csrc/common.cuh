@@ -9,6 +9,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pagedkv.h"
@@ -172,6 +173,36 @@ struct RowLoad {
         f[2 * i] = x.x;
         f[2 * i + 1] = x.y;
       }
+    }
+  }
+};
+
+// One row fragment of a cache page: N consecutive elements widened to float.
+// 16- and 32-bit pools use RowLoad; FP8 E4M3 codes are widened two at a
+// time through CUDA's e4m3x2 -> half2 conversion (exact: every E4M3 value
+// is a half).
+template <typename TC, int N>
+struct CacheRow {
+  static __device__ __forceinline__ void load(const TC* p, float (&f)[N]) { RowLoad<TC, N>::load(p, f); }
+};
+
+__device__ __forceinline__ float2 e4m3x2_to_float2(uint16_t x) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)x, __NV_E4M3);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+template <int N>
+struct CacheRow<__nv_fp8_e4m3, N> {
+  static_assert(N == 2 || N == 4, "FP8 row fragment size");
+  static __device__ __forceinline__ void load(const __nv_fp8_e4m3* p, float (&f)[N]) {
+    if constexpr (N == 4) {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(p);
+      const float2 a = e4m3x2_to_float2((uint16_t)(w & 0xffffu));
+      const float2 b = e4m3x2_to_float2((uint16_t)(w >> 16));
+      f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+    } else {
+      const float2 a = e4m3x2_to_float2(*reinterpret_cast<const uint16_t*>(p));
+      f[0] = a.x; f[1] = a.y;
     }
   }
 };

@@ -46,6 +46,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -69,6 +70,8 @@ struct DecodeParams {
   float2* ws_ml;     // [S][H][num_parts] (m, l), used when num_parts > 1
   float* ws_o;       // [S][H][num_parts][D]
   unsigned* err;
+  const float* k_scale;  // FP8 pools: per-KV-head scales (else unused)
+  const float* v_scale;
 };
 
 constexpr int kMaxPartSize = 8192;
@@ -77,7 +80,7 @@ constexpr int cmin(int a, int b) { return a < b ? a : b; }
 constexpr int cmax(int a, int b) { return a > b ? a : b; }
 constexpr int clog2(int x) { return x <= 1 ? 0 : 1 + clog2(x / 2); }
 
-template <typename T, int D, int BS, int G>
+template <typename T, int D, int BS, int G, typename TC = T>
 struct DecodeCfg {
   // Shape chosen by measurement on GB300: small rings (two 8-position stages
   // per warp, 32 KiB per CTA) let up to 7 CTAs share an SM, and the extra
@@ -90,7 +93,7 @@ struct DecodeCfg {
   static constexpr int kLanesPerPos = 32 / kChunk;          // after the reduce-scatter
   static constexpr int kShift = clog2(kLanesPerPos);
   static constexpr int kDpl = D / 32;                       // elements per lane
-  static constexpr int kChunkBytes = kChunk * D * (int)sizeof(T);
+  static constexpr int kChunkBytes = kChunk * D * (int)sizeof(TC);
   static constexpr int kStageBytes = 2 * kChunkBytes;       // keys + values
   static constexpr int kRingBudget = 32 * 1024;
   static constexpr int kStages = cmax(2, cmin(8, kRingBudget / (kWarps * kStageBytes)));
@@ -129,10 +132,14 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[C], int lane) {
   return x;
 }
 
-template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G>::kThreads)
+// T: type of q and out; TC: type of the cache elements (T itself, or FP8
+// E4M3 codes whose per-head scales are folded into the query and the
+// output).
+template <typename T, int D, int BS, int G, typename TC = T>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, G, TC>::kThreads)
 decode_partition_kernel(const DecodeParams p) {
-  using Cfg = DecodeCfg<T, D, BS, G>;
+  using Cfg = DecodeCfg<T, D, BS, G, TC>;
+  constexpr bool kScaled = !std::is_same<T, TC>::value;
   constexpr int C = Cfg::kChunk;
   constexpr int NW = Cfg::kWarps;
   constexpr int NST = Cfg::kStages;
@@ -221,7 +228,7 @@ decode_partition_kernel(const DecodeParams p) {
     const int st = j % NST;
     const int pb = stable[c / CPB];
     const int64_t row = ((int64_t)pb * p.kv_heads + kvh) * BS + (c % CPB) * C;
-    const int64_t off = row * D * (int64_t)sizeof(T);
+    const int64_t off = row * D * (int64_t)sizeof(TC);  // bytes: cache element size
     const uint32_t bar = bar0 + st * 8;
     const uint32_t dst = ring0 + st * Cfg::kStageBytes;
     mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
@@ -234,15 +241,17 @@ decode_partition_kernel(const DecodeParams p) {
   }
 
   // Query rows of the group, pre-scaled into base-2 score units (loaded while
-  // the first copies are in flight).
+  // the first copies are in flight); an FP8 key scale folds in here.
   float qv[G][DPL];
   {
+    float qs = p.qscale;
+    if constexpr (kScaled) qs *= p.k_scale[kvh];
     const T* qp = static_cast<const T*>(p.q) + out0 + lane * DPL;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       RowLoad<T, DPL>::load(qp + g * D, qv[g]);
 #pragma unroll
-      for (int d = 0; d < DPL; ++d) qv[g][d] *= p.qscale;
+      for (int d = 0; d < DPL; ++d) qv[g][d] *= qs;
     }
   }
 
@@ -266,8 +275,8 @@ decode_partition_kernel(const DecodeParams p) {
     if (timed_out) break;
     const int c = warp + j * NW;
     const int nvalid = min(C, ntok - c * C);
-    const T* ks = reinterpret_cast<const T*>(smem + (warp * NST + st) * Cfg::kStageBytes);
-    const T* vs = ks + C * D;
+    const TC* ks = reinterpret_cast<const TC*>(smem + (warp * NST + st) * Cfg::kStageBytes);
+    const TC* vs = ks + C * D;
 
     // ---- scores ------------------------------------------------------
     float sc[G];
@@ -276,7 +285,7 @@ decode_partition_kernel(const DecodeParams p) {
 #pragma unroll
       for (int t = 0; t < C; ++t) {
         float kf[DPL];
-        RowLoad<T, DPL>::load(ks + t * D + lane * DPL, kf);
+        CacheRow<TC, DPL>::load(ks + t * D + lane * DPL, kf);
 #pragma unroll
         for (int g = 0; g < G; ++g) {
           float a = 0.f;
@@ -317,7 +326,7 @@ decode_partition_kernel(const DecodeParams p) {
         if (t < nvalid) {
           const float pt = __shfl_sync(kFullMask, sc[0], t << SH);
           float vf[DPL];
-          RowLoad<T, DPL>::load(vs + t * D + lane * DPL, vf);
+          CacheRow<TC, DPL>::load(vs + t * D + lane * DPL, vf);
 #pragma unroll
           for (int d = 0; d < DPL; ++d) acc[0][d] = fmaf(pt, vf[d], acc[0][d]);
         }
@@ -343,7 +352,7 @@ decode_partition_kernel(const DecodeParams p) {
             }
           }
           float vf[DPL];
-          RowLoad<T, DPL>::load(vs + t * D + lane * DPL, vf);
+          CacheRow<TC, DPL>::load(vs + t * D + lane * DPL, vf);
 #pragma unroll
           for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -402,6 +411,8 @@ decode_partition_kernel(const DecodeParams p) {
     fin[G + g] = tot;
   }
   __syncthreads();
+  float vscale = 1.f;
+  if constexpr (kScaled) vscale = p.v_scale[kvh];  // FP8 value scale, applied once
   for (int e = threadIdx.x; e < G * D; e += Cfg::kThreads) {
     const int g = e / D;
     const int d = e - g * D;
@@ -409,6 +420,7 @@ decode_partition_kernel(const DecodeParams p) {
 #pragma unroll
     for (int w = 0; w < NW; ++w) o = fmaf(red_acc[(w * G + g) * D + d], fac[w * G + g], o);
     o = o / fin[G + g];
+    if constexpr (kScaled) o *= vscale;
     if (nparts == 1)
       out[out0 + e] = Elem<T>::from_f(o);
     else

@@ -8,6 +8,7 @@
 
 #include "decode.cuh"
 #include "decode_mma.cuh"
+#include "decode_mma_fp8.cuh"
 
 namespace pkv {
 
@@ -39,6 +40,19 @@ int allow_smem(K kern, int bytes) {
   return PKV_OK;
 }
 
+// The split-K merge, when any sequence spans several partitions.
+template <typename T, int D>
+void launch_reduce(const DecodeParams& p, int num_seqs, cudaStream_t stream) {
+  if (p.num_parts <= 1) return;
+  if (p.num_parts <= 8) {
+    dim3 g2((unsigned)((p.num_heads + kReduceWarps - 1) / kReduceWarps), (unsigned)num_seqs);
+    decode_reduce_kernel<T, D, 1><<<g2, kReduceWarps * 32, 0, stream>>>(p);
+  } else {
+    dim3 g2((unsigned)p.num_heads, (unsigned)num_seqs);
+    decode_reduce_kernel<T, D, kReduceWarps><<<g2, kReduceWarps * 32, 0, stream>>>(p);
+  }
+}
+
 template <typename T, int D, int BS, int G>
 int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* maps,
                       cudaStream_t stream) {
@@ -59,16 +73,52 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* map
     if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
     kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
   }
-  if (p.num_parts > 1) {
-    if (p.num_parts <= 8) {
-      dim3 g2((unsigned)((p.num_heads + kReduceWarps - 1) / kReduceWarps), (unsigned)num_seqs);
-      decode_reduce_kernel<T, D, 1><<<g2, kReduceWarps * 32, 0, stream>>>(p);
-    } else {
-      dim3 g2((unsigned)p.num_heads, (unsigned)num_seqs);
-      decode_reduce_kernel<T, D, kReduceWarps><<<g2, kReduceWarps * 32, 0, stream>>>(p);
-    }
-  }
+  launch_reduce<T, D>(p, num_seqs, stream);
   return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// FP8 pools (T is the 16-bit type of q and out): the tensor-core kernel
+// that widens codes in shared memory, or the CUDA-core kernel.
+template <typename T, int D, int BS, int G>
+int launch_decode_fp8_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* maps,
+                          bool mma, cudaStream_t stream) {
+  dim3 grid((unsigned)p.kv_heads, (unsigned)num_seqs, (unsigned)p.num_parts);
+  if (mma && D == 128) {
+    if (!maps) return PKV_ERR_CUDA;
+    if constexpr (D == 128) {
+      using Cfg = Fp8MmaCfg<T, D, BS, G>;
+      auto kern = decode_partition_mma_fp8_kernel<T, D, BS, G>;
+      if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
+      kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p, maps->k, maps->v);
+    }
+  } else if (mma) {
+    using Cfg = Fp8WidenCfg<T, D, BS, G>;
+    auto kern = decode_partition_mma_fp8_widen_kernel<T, D, BS, G>;
+    if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
+    kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
+  } else {
+    using Cfg = DecodeCfg<T, D, BS, G, __nv_fp8_e4m3>;
+    auto kern = decode_partition_kernel<T, D, BS, G, __nv_fp8_e4m3>;
+    if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
+    kern<<<grid, Cfg::kThreads, Cfg::smem_bytes(p.part_size), stream>>>(p);
+  }
+  launch_reduce<T, D>(p, num_seqs, stream);
+  return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <typename T>
+int launch_decode_fp8(const DecodeParams& p, int num_seqs, int head_dim, int block_size, int group,
+                      const DecodeMaps* maps, bool mma, cudaStream_t stream) {
+#define PKV_FP8_CASE(D_, B_, G_)                   \
+  if (head_dim == D_ && block_size == B_ && group == G_) \
+    return launch_decode_fp8_cfg<T, D_, B_, G_>(p, num_seqs, maps, mma, stream);
+#define PKV_FP8_G(D_, B_) PKV_FP8_CASE(D_, B_, 1) PKV_FP8_CASE(D_, B_, 2) \
+  PKV_FP8_CASE(D_, B_, 4) PKV_FP8_CASE(D_, B_, 8)
+  PKV_FP8_G(64, 8) PKV_FP8_G(64, 16) PKV_FP8_G(64, 32) PKV_FP8_G(64, 64)
+  PKV_FP8_G(128, 8) PKV_FP8_G(128, 16) PKV_FP8_G(128, 32) PKV_FP8_G(128, 64)
+#undef PKV_FP8_G
+#undef PKV_FP8_CASE
+  return PKV_ERR_GEOMETRY;
 }
 
 template <typename T, int D, int BS>

@@ -18,8 +18,9 @@ workloads extend those shapes to grouped heads, forks and long contexts.
 import numpy as np
 import torch
 
-TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+TORCH_DTYPE = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16,
+               "e4m3": torch.float8_e4m3fn}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 # name -> shape of one decode step.  Lengths are cached tokens *before* the
 # step; the step writes one token per sequence at position T_i and attends
@@ -100,9 +101,22 @@ def normal(seed, shape, dtype, device="cpu"):
     return x.to(TORCH_DTYPE[dtype])
 
 
+def random_codes(seed, shape, device="cpu"):
+    """Seeded random bytes for an 8-bit E4M3 pool, avoiding the two bytes
+    that encode NaN (0x7F, 0xFF)."""
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    mag = torch.randint(0, 0x7F, shape, generator=gen, device=device, dtype=torch.int32)
+    sign = torch.randint(0, 2, shape, generator=gen, device=device, dtype=torch.int32) * 0x80
+    return (mag | sign).to(torch.uint8).view(torch.float8_e4m3fn)
+
+
 def storage_numpy(t, dtype):
-    """Host NumPy copy of a tensor in its stored form (bf16 as uint16 bits)."""
+    """Host NumPy copy of a tensor in its stored form (bf16 as uint16 bits,
+    E4M3 as uint8 codes)."""
     t = t.detach().cpu().contiguous()
     if dtype == "bf16":
         return t.view(torch.int16).numpy().view(np.uint16)
+    if dtype == "e4m3":
+        return t.view(torch.uint8).numpy()
     return t.numpy()

@@ -47,7 +47,7 @@ def test_strerror_covers_codes(lib):
 
 def fake_cache(**kw):
     c = dict(k_cache=0x10000, v_cache=0x20000, num_blocks=32, block_size=16, num_kv_heads=4,
-             head_dim=64, dtype=_lib.PKV_F32)
+             head_dim=64, dtype=_lib.PKV_F32, k_scale=0x80000, v_scale=0x90000, io_dtype=_lib.PKV_F32)
     c.update(kw)
     return _lib.pkv_cache(**c)
 
@@ -69,6 +69,9 @@ def test_write_argument_errors(lib):
     assert lib.paged_kv_write(None, P(1), P(1), P(1), 1, None) == -1
     assert write(lib, fake_cache(k_cache=0)) == -1
     assert write(lib, fake_cache(dtype=7)) == -3
+    # FP8 pools need both scales and a 16-bit io type.
+    assert write(lib, fake_cache(dtype=_lib.PKV_FP8_E4M3, io_dtype=_lib.PKV_F32)) == -3
+    assert write(lib, fake_cache(dtype=_lib.PKV_FP8_E4M3, io_dtype=_lib.PKV_F16, k_scale=0)) == -1
     assert write(lib, fake_cache(num_blocks=0)) == -3
     assert write(lib, fake_cache(head_dim=3)) == -2        # 12-byte rows
     assert write(lib, fake_cache(k_cache=0x10008)) == -4
