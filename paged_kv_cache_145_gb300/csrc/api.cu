@@ -95,8 +95,30 @@ int resolve_max_len(const pkv_cache* c, int32_t max_blocks, int32_t max_seq_len)
   return max_seq_len;
 }
 
-int resolve_partition(const pkv_cache* c, int32_t requested) {
-  if (requested == 0) return kDefaultPartition;
+// Default partition length.  16-bit and 32-bit pools use 512 positions.
+// An FP8 partition carries half the bytes per position, so its fixed costs
+// (table staging, first-load latency, the split-K merge) weigh twice as
+// much: FP8 pools take the longest of 2048, 1024 and 512 positions that
+// still launches at least 12 thread blocks per SM (sequences x KV heads x
+// partitions), so large batches skip the split while few long sequences
+// keep every SM busy.
+int default_partition(const pkv_cache* c, int64_t num_seqs, int64_t max_len) {
+  if (c->dtype != PKV_FP8_E4M3 || num_seqs < 1 || max_len < 1) return kDefaultPartition;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1) {
+    cudaGetLastError();
+    return kDefaultPartition;
+  }
+  for (int part = 2048; part > kDefaultPartition; part /= 2) {
+    const int64_t blocks = num_seqs * c->num_kv_heads * ((max_len + part - 1) / part);
+    if (blocks >= 12LL * sms) return part;
+  }
+  return kDefaultPartition;
+}
+
+int resolve_partition(const pkv_cache* c, int32_t requested, int64_t num_seqs, int64_t max_len) {
+  if (requested == 0) return default_partition(c, num_seqs, max_len);
   if (requested < c->block_size || requested % c->block_size || requested > pkv::kMaxPartSize)
     return PKV_ERR_ARG;
   return requested;
@@ -212,14 +234,14 @@ int32_t paged_attention_partition_size(const pkv_cache* cache, int32_t num_seqs,
                                        int32_t requested) {
   if (!cache) return PKV_ERR_NULL;
   if (num_seqs < 0 || num_heads < 1 || max_seq_len < 0) return PKV_ERR_ARG;
-  return resolve_partition(cache, requested);
+  return resolve_partition(cache, requested, num_seqs, max_seq_len);
 }
 
 size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
                                        int32_t num_heads, int32_t max_seq_len,
                                        int32_t partition_size) {
   if (!cache || num_seqs < 1 || num_heads < 1 || max_seq_len < 1) return 0;
-  const int part = resolve_partition(cache, partition_size);
+  const int part = resolve_partition(cache, partition_size, num_seqs, max_seq_len);
   if (part < 0) return 0;
   return workspace_layout(num_seqs, num_heads, cache->head_dim, max_seq_len, part).total;
 }
@@ -244,7 +266,7 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
     return PKV_ERR_ALIGN;
   const int max_len = resolve_max_len(cache, max_blocks_per_seq, max_seq_len);
   if (max_len < 1) return PKV_ERR_ARG;
-  const int part = resolve_partition(cache, partition_size);
+  const int part = resolve_partition(cache, partition_size, num_seqs, max_len);
   if (part < 0) return part;
   const WsLayout ws = workspace_layout(num_seqs, num_heads, cache->head_dim, max_len, part);
   if (ws.parts > 65535) return PKV_ERR_ARG;  // partitions index the grid's z dimension

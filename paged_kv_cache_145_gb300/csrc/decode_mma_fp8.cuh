@@ -400,31 +400,29 @@ decode_partition_mma_fp8_widen_kernel(const DecodeParams p) {
 template <typename T, int D, int BS, int G>
 struct Fp8MmaCfg {
   static constexpr int kWarps = 4;
+  static constexpr int kMinBlocks = 4;  // CTAs per SM the register budget targets
   static constexpr int kThreads = kWarps * 32;
   static constexpr int kChunk = 16;
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kRawBytes = kChunk * D;            // 16 rows x 128 codes, swizzled
   static constexpr int kRawStage = 2 * kRawBytes;         // keys + values
-  static constexpr int kStages = 2;
-  static constexpr int kBoxBytes = kChunk * 128;          // 16-bit value tile: 16 rows x 128 B
-  static constexpr int kVTileBytes = (D / 64) * kBoxBytes;
+  static constexpr int kStages = 2;  // raw stages per warp
   static constexpr int kRingBytes = kWarps * kStages * kRawStage;
-  static constexpr int kVOff = kRingBytes;
-  static constexpr int kBarOff = kVOff + kWarps * kVTileBytes;
+  static constexpr int kBarOff = kRingBytes;
   static constexpr int kPtOff = kBarOff + kWarps * kStages * 8;
   static constexpr int kPtBytes = 8 * kChunk * 2;
   static constexpr int kTableOff = kPtOff + kWarps * kPtBytes;
   static constexpr int kAlign = 1024;
   static constexpr int kMergeBytes = (kWarps * G * D + 3 * kWarps * G + 2 * G) * 4;
   static_assert(D == 128, "direct key fragments need 128-byte code rows");
-  static_assert(kMergeBytes <= kRingBytes + kWarps * kVTileBytes, "merge scratch");
+  static_assert(kMergeBytes <= kRingBytes, "merge scratch");
   static_assert(BS % 16 == 0 || 16 % BS == 0, "block size");
   static constexpr int smem_bytes(int part_size) { return kAlign + kTableOff + (part_size / BS) * 4; }
   static constexpr int kMaxSmem = kAlign + kTableOff + (kMaxPartSize / BS) * 4;
 };
 
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(Fp8MmaCfg<T, D, BS, G>::kThreads)
+__global__ void __launch_bounds__(Fp8MmaCfg<T, D, BS, G>::kThreads, Fp8MmaCfg<T, D, BS, G>::kMinBlocks)
 decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap tmk,
                                 const __grid_constant__ CUtensorMap tmv) {
   using Cfg = Fp8MmaCfg<T, D, BS, G>;
@@ -575,9 +573,6 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
   const int mm = lane >> 3, mr = lane & 7;
   const int k_row = (mm & 1) * 8 + mr;  // ldmatrix row this lane addresses (keys)
   const int k_half = mm >> 1;           // which 16-code chunk of the pair
-  const int v_tok = (mm >> 1) * 8 + mr, v_col8 = mm & 1;
-  unsigned char* vtw = smem + Cfg::kVOff + warp * Cfg::kVTileBytes;
-  const uint32_t vtile = smem_addr(vtw);
   uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
 
   int j = 0;
@@ -589,29 +584,6 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
     const int nvalid = min(C, ntok - c * C);
     const uint32_t kraw = raw0 + st * Cfg::kRawStage;
     const unsigned char* vraw = smem + (kraw - smem_addr(smem)) + Cfg::kRawBytes;
-
-    // ---- widen the values into the swizzled fp16 tile ---------------------
-    // Lane: code chunk cc (dims 16cc .. 16cc+15) of row r, where lanes with
-    // cc >= 4 take row r ^ 1: each 8-lane phase then reads and writes eight
-    // distinct bank groups (the swizzle XOR differs between the two rows).
-    {
-      const int cc = lane & 7;
-      const int box = cc >> 2, c8 = (cc & 3) * 2;
-#pragma unroll
-      for (int pass = 0; pass < 4; ++pass) {
-        const int r = (pass * 4 + (lane >> 3)) ^ box;
-        const uint4 vc = *reinterpret_cast<const uint4*>(vraw + r * 128 + ((cc ^ (r & 7)) << 4));
-        uint4 v0, v1;
-        e4m3x4_to_f16x4(vc.x, v0.x, v0.y);
-        e4m3x4_to_f16x4(vc.y, v0.z, v0.w);
-        e4m3x4_to_f16x4(vc.z, v1.x, v1.y);
-        e4m3x4_to_f16x4(vc.w, v1.z, v1.w);
-        if (r >= nvalid) v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
-        unsigned char* vr = vtw + box * Cfg::kBoxBytes + r * 128;
-        *reinterpret_cast<uint4*>(vr + ((c8 ^ (r & 7)) << 4)) = v0;
-        *reinterpret_cast<uint4*>(vr + (((c8 + 1) ^ (r & 7)) << 4)) = v1;
-      }
-    }
 
     // ---- S^T = K . Q^T, key fragments straight from the codes -------------
     float sc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -628,11 +600,6 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
         e4m3x4_to_f16x4(r[2 * h + 1], a[1], a[3]);
         Op::run(sc, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
       }
-    }
-    __syncwarp();
-    if (lane == 0 && j + NST < count) {  // raw stage consumed: refill it
-      fence_proxy_async();
-      issue(j + NST);
     }
 
     // ---- online softmax per head column ------------------------------------
@@ -678,17 +645,42 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
     const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
     const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
 
-    // ---- O^T += V^T . P^T (fp16) -------------------------------------------
+    // ---- O^T += V^T . P^T, value fragments straight from the codes --------
+    // The contraction runs over positions, which sit in different code rows,
+    // so each lane gathers a 4 x 4 byte block: dims 4w .. 4w+3 (w = gi + 8q)
+    // of rows 2ti, 2ti+1, 2ti+8, 2ti+9 (four 32-bit loads that hit 32
+    // distinct banks under the 128-byte swizzle), pairs the bytes of two
+    // rows per dim with byte permutes and widens them to fp16.  The M rows
+    // of the two tiles of group q are dims 4w, 4w+1 (tile 2q) and 4w+2,
+    // 4w+3 (tile 2q+1); the merge below undoes that order.
+    {
+      const int r0 = 2 * ti;
+      const bool ok0 = r0 < nvalid, ok1 = r0 + 1 < nvalid, ok2 = r0 + 8 < nvalid,
+                 ok3 = r0 + 9 < nvalid;
 #pragma unroll
-    for (int i = 0; i < KSTEPS; ++i) {
-      const int col8 = 2 * (i % 4) + v_col8;
-      const uint32_t addr =
-          vtile + (i / 4) * Cfg::kBoxBytes + v_tok * 128 + ((col8 ^ (v_tok & 7)) << 4);
-      uint32_t a[4];
-      ldsm_x4_trans(a, addr);
-      Op::run(acc[i], a, b0, b1);
+      for (int q = 0; q < D / 32; ++q) {
+        const int w = gi + 8 * q;
+        const int ch = w >> 2, wo = (w & 3) * 4;
+        auto word = [&](int r, bool ok) -> uint32_t {
+          return ok ? *reinterpret_cast<const uint32_t*>(vraw + r * 128 + ((ch ^ (r & 7)) << 4) + wo)
+                    : 0u;
+        };
+        const uint32_t x0 = word(r0, ok0), x1 = word(r0 + 1, ok1);
+        const uint32_t x2 = word(r0 + 8, ok2), x3 = word(r0 + 9, ok3);
+        uint32_t a[4], b[4];
+        e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x5140), a[0], a[1]);
+        e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x5140), a[2], a[3]);
+        e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x7362), b[0], b[1]);
+        e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x7362), b[2], b[3]);
+        Op::run(acc[2 * q], a, b0, b1);
+        Op::run(acc[2 * q + 1], b, b0, b1);
+      }
     }
-    __syncwarp();  // the value tile and P^T are rewritten next chunk
+    __syncwarp();  // the raw stage and P^T are rewritten next
+    if (lane == 0 && j + NST < count) {  // raw stage consumed: refill it
+      fence_proxy_async();
+      issue(j + NST);
+    }
   }
   if (timed_out) {
     const int last = count < j + NST ? count : j + NST;
@@ -704,14 +696,14 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
   float* red_l = red_m + NW * G;
   float* fac = red_l + NW * G;
   float* fin = fac + NW * G;
+  // Lane (gi, ti) holds dims 4w .. 4w+3 (w = gi + 8q) of heads 2ti, 2ti+1.
 #pragma unroll
-  for (int i = 0; i < KSTEPS; ++i)
+  for (int q = 0; q < D / 32; ++q)
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      const int head = 2 * ti + (cc & 1);
-      const int dim = 16 * i + gi + 8 * (cc >> 1);
-      if (head < G) red_acc[(warp * G + head) * D + dim] = acc[i][cc];
-    }
+    for (int h = 0; h < 2; ++h)
+      if (2 * ti + h < G)
+        *reinterpret_cast<float4*>(&red_acc[(warp * G + 2 * ti + h) * D + 4 * (gi + 8 * q)]) =
+            make_float4(acc[2 * q][h], acc[2 * q][2 + h], acc[2 * q + 1][h], acc[2 * q + 1][2 + h]);
   if (gi == 0) {
 #pragma unroll
     for (int h = 0; h < 2; ++h)

@@ -33,17 +33,17 @@ CONFIGS = {
               "permuted blocks, 4 sequences of lengths {50, 20, 65, 1}"),
     "opt13b": dict(
         index=1, heads=40, kv_heads=40, head_dim=128, dtype="f16", block_size=16,
-        batch=64, len_lo=200, len_hi=2000, slack=0.10,
+        layers=40, batch=64, len_lo=200, len_hi=2000, slack=0.10,
         about="OPT-13B-shaped decode: 40 heads MHA, head_dim 128, fp16, block 16, "
               "batch 64, context lengths U{200..2000}, shuffled pool = need + 10%"),
     "gqa": dict(
         index=2, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
-        batch=256, len_lo=200, len_hi=2000, slack=0.10,
+        layers=32, batch=256, len_lo=200, len_hi=2000, slack=0.10,
         about="Llama-3-8B-shaped GQA decode: 32 query / 8 KV heads, head_dim 128, "
               "bf16, block 16, batch 256, context lengths U{200..2000}"),
     "fork": dict(
         index=3, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
-        groups=16, forks=8, prompt=1031, slack=0.10,
+        layers=32, groups=16, forks=8, prompt=1031, slack=0.10,
         about="parallel sampling: 16 groups x 8 forks sharing a 1031-token prompt "
               "(last block partial), GQA 32/8, head_dim 128, bf16, block 16"),
     "prefill": dict(
@@ -58,7 +58,7 @@ CONFIGS = {
               "chunk, GQA 32/8, head_dim 128, bf16, block 16, causal"),
     "long": dict(
         index=4, heads=32, kv_heads=8, head_dim=128, dtype="bf16", block_size=16,
-        batch=8, len_lo=16384, len_hi=32768, slack=0.10, partition_size=512,
+        layers=32, batch=8, len_lo=16384, len_hi=32768, slack=0.10, partition_size=512,
         about="long-context split-K: GQA 32/8, head_dim 128, bf16, batch 8, "
               "context lengths U{16384..32768}, 512-token partitions"),
 }

@@ -32,6 +32,20 @@ def test_workload_plans_one_new_position_per_sequence():
     assert len(f.pairs) == 16 * 7
 
 
+def test_unique_bytes_count_shared_pages_once():
+    # Parallel sampling: each group's 64 full prompt blocks are shared by its
+    # 8 forks; copy-on-write gave 7 forks a private copy of the partial last
+    # block and the 8th kept the original, each now holding 8 positions.
+    f = bench.Workload("fork")
+    per_pos = 2 * 8 * 128 * 2
+    assert f.unique_kv_bytes() == 16 * (64 * 16 + 8 * 8) * per_pos
+    _, logical = f.decode_bytes(512)
+    assert logical == 16 * 8 * 1032 * per_pos
+    # No sharing: unique equals logical.
+    w = bench.Workload("opt13b")
+    assert w.unique_kv_bytes() == w.decode_bytes(512)[1]
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))

@@ -153,6 +153,25 @@ def test_fp8_prefill_is_refused():
                                     torch.tensor([3], dtype=torch.int32).cuda(), 0.1, 3)
 
 
+def test_fp8_default_partition_follows_grid_size():
+    """FP8 pools default to the longest of 2048 / 1024 / 512 positions that
+    still launches 12 thread blocks per SM; 16-bit pools keep 512."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cache = fp8_cache(4, 8, 16, 128, "bf16", 5)
+
+    def expect(S, L):
+        for part in (2048, 1024):
+            if S * 8 * -(-L // part) >= 12 * sms:
+                return part
+        return 512
+
+    for S, L in [(256, 2001), (64, 2001), (8, 32768), (1, 100), (4096, 3000)]:
+        assert pkv.paged_attention_partition_size(cache, S, 32, L) == expect(S, L)
+    native = pkv.PagedKVCache(torch.zeros(4, 8, 16, 128, dtype=torch.bfloat16, device="cuda"),
+                              torch.zeros(4, 8, 16, 128, dtype=torch.bfloat16, device="cuda"))
+    assert pkv.paged_attention_partition_size(native, 256, 32, 2001) == 512
+
+
 def test_fp8_bf16_queries_beyond_fp16_range(kernel):
     """bf16 queries up to ~5e5 (past fp16's 65504) with a small key scale:
     the scores stay O(1) and the output must still match the oracle, so the
