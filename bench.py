@@ -13,6 +13,12 @@ The default workload is the OPT-13B-shaped decode (40 heads MHA, head_dim
 the pool (about 1.6 GB) is larger than L2, so no flush is needed between
 steps.
 
+The timed region runs K steps back to back (device time between one event
+before the first and one after the last) and then K decode launches alone,
+whose mean duration is the roofline's per-launch time.  Pools smaller than
+twice L2 (the parallel-sampling workload) are flushed before every step and
+every decode launch, and each is bracketed by its own events.
+
 Under torchrun (N > 1) every rank runs its own batch on its own GPU with no
 collective on the data path (sequences are independent: weak scaling); the
 timed region is bracketed by barriers and the slowest rank's time is used.
@@ -43,24 +49,24 @@ from paged_kv_cache_145_gb300 import synth  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
 
-# DRAM bytes (read + write) per launch of the decode kernels, from ncu
-# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and KV
-# dtype, with the hash of the kernel sources they were taken on.  A stale
-# hash reports null.
+# DRAM bytes (read + write) per launch of the decode partition kernel, from
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and
+# KV dtype, with the hash of the sources of that kernel family they were
+# taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b": (1280275968, "efd6c816a71e6062"),
-    "gqa": (1128982784, "efd6c816a71e6062"),
-    "opt13b/fp8": (645104896, "efd6c816a71e6062"),
-    "gqa/fp8": (568320256, "efd6c816a71e6062"),
+    "opt13b": (1280275968, "118000bf3980d6e6"),
+    "gqa": (1128982784, "118000bf3980d6e6"),
 }
 
-KERNEL_SOURCES = ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_mma_fp8.cuh",
-                  "decode_launch.cuh")
+KERNEL_SOURCES = {
+    "native": ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh"),
+    "fp8": ("common.cuh", "decode.cuh", "decode_mma_fp8.cuh", "decode_launch.cuh", "api.cu"),
+}
 
 
-def kernel_source_hash():
+def kernel_source_hash(family="native"):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "paged_kv_cache_145_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -393,18 +399,20 @@ def run_ours(args):
     scale = 1.0 / math.sqrt(w.D)
     has_pairs = len(w.pairs) > 0
     nparts_max = -(-w.max_len // part)
-    launches_per_step = 1 + 1 + (1 if nparts_max > 1 else 0) + (1 if has_pairs else 0)
+    decode_launches = 1 + (1 if nparts_max > 1 else 0)
+    launches_per_step = 1 + decode_launches + (1 if has_pairs else 0)
 
     stream = torch.cuda.current_stream()
 
-    def step(mid=None):
+    def decode():
+        pkv.paged_attention_decode(cache, q, tables, lens, scale, out=out, max_seq_len=w.max_len,
+                                   workspace=ws, partition_size=part)
+
+    def step():
         if has_pairs:
             pkv.paged_block_copy(cache, pairs)
         pkv.paged_kv_write(cache, k, v, slots)
-        if mid is not None:
-            mid.record(stream)
-        pkv.paged_attention_decode(cache, q, tables, lens, scale, out=out, max_seq_len=w.max_len,
-                                   workspace=ws, partition_size=part)
+        decode()
 
     for _ in range(args.warmup):
         step()
@@ -419,29 +427,41 @@ def run_ours(args):
     flush_l2 = w.pool_bytes() < 2 * l2_bytes
     flush_buf = torch.empty(2 * l2_bytes, dtype=torch.uint8, device=dev) if flush_l2 else None
 
+    def span(fn, n, flush):
+        """Device time of n calls of fn.  Without a flush only the first
+        and last call are bracketed by events (an event record between two
+        kernels costs about 2 us of device time); with a flush every call is
+        bracketed and the flushes are left out."""
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n if flush else 1)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n if flush else 1)]
+        for i in range(n):
+            if flush:
+                flush_buf.fill_(i & 0xFF)
+            if flush or i == 0:
+                e0[i if flush else 0].record(stream)
+            fn()
+            if flush or i == n - 1:
+                e1[i if flush else 0].record(stream)
+        return e0, e1
+
+    def elapsed(e0, e1):
+        return sum(a.elapsed_time(b) for a, b in zip(e0, e1))
+
     def timed(n, flush, sampler=None):
-        starts = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        mids = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
-        ends = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        """The timed region: n steps, then n decode launches alone (the
+        roofline's per-launch duration), between barriers and syncs."""
         barrier()
         torch.cuda.synchronize()
         if sampler is not None:
             sampler.start()
             time.sleep(0.3)  # let the sampler start before the timed region
-        for i in range(n):
-            if flush:
-                flush_buf.fill_(i & 0xFF)
-            starts[i].record(stream)
-            step(mids[i])
-            ends[i].record(stream)
+        steps = span(step, n, flush)
+        decodes = span(decode, n, flush)
         torch.cuda.synchronize()
         barrier()
         clk = sampler.stop() if sampler is not None else None
         assert pkv.paged_get_device_error() == 0
-        total = (sum(starts[i].elapsed_time(ends[i]) for i in range(n)) if flush
-                 else starts[0].elapsed_time(ends[-1]))
-        dec = statistics.fmean(mids[i].elapsed_time(ends[i]) for i in range(n))
-        return total, dec, clk
+        return elapsed(*steps), elapsed(*decodes) / n, clk
 
     total_ms, decode_ms, clocks = timed(args.steps, flush_l2, ClockSampler(local_rank))
     warm = timed(args.steps, False) if flush_l2 else None
@@ -493,7 +513,7 @@ def run_ours(args):
     roof_bytes = dec_bytes - kv_bytes + unique_bytes
     achieved = roof_bytes / (decode_ms / 1e3) / 1e9
     layers = w.cfg.get("layers", 1)
-    src_hash = kernel_source_hash()
+    src_hash = kernel_source_hash("fp8" if kv_dtype else "native")
     default_shape = args.partition == 0 and args.block_size == 0 and args.table == "shuffled"
     tr = TRAFFIC.get(args.config + ("/fp8" if kv_dtype else "")) if default_shape else None
     traffic = tr[0] if tr and tr[1] == src_hash else None
@@ -537,7 +557,7 @@ def run_ours(args):
                      "basis": ("distinct positions (shared pages counted once)"
                                if unique_bytes < kv_bytes else "every position read")},
         "clocks": clocks,
-        "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches": (launches_per_step + decode_launches) * args.steps,
         "e2e": {"value": round(all_e2e_bytes / max_e2e_s / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5)},
