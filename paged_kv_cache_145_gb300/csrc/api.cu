@@ -26,6 +26,10 @@ int pkv_launch_prefill_f16(const pkv::PrefillParams&, int, int, int, int, const 
                            const CUtensorMap&, cudaStream_t);
 int pkv_launch_prefill_bf16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
                             const CUtensorMap&, cudaStream_t);
+int pkv_launch_prefill_tc_f16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
+                              const CUtensorMap&, cudaStream_t);
+int pkv_launch_prefill_tc_bf16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
+                               const CUtensorMap&, cudaStream_t);
 int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
                           cudaStream_t);
 int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
@@ -151,6 +155,13 @@ WsLayout workspace_layout(int num_seqs, int num_heads, int head_dim, int max_len
 bool simt_forced() {
   const char* env = std::getenv("PKV_DECODE_KERNEL");
   return env && std::strcmp(env, "simt") == 0;
+}
+
+// Prefill runs on the tcgen05 kernel; PKV_PREFILL_KERNEL=mma in the
+// environment selects the mma.sync kernel instead (read on every call).
+bool prefill_mma_forced() {
+  const char* env = std::getenv("PKV_PREFILL_KERNEL");
+  return env && std::strcmp(env, "mma") == 0;
 }
 
 bool use_mma(const pkv_cache* c, int group) {
@@ -374,11 +385,13 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
   p.qscale = scale * 1.4426950408889634f;
   p.err = err;
   const int group = num_heads / cache->num_kv_heads;
-  if (cache->dtype == PKV_F16)
-    return pkv_launch_prefill_f16(p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv,
-                                  stream);
-  return pkv_launch_prefill_bf16(p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv,
-                                 stream);
+  const bool f16 = cache->dtype == PKV_F16;
+  if (prefill_mma_forced())
+    return (f16 ? pkv_launch_prefill_f16 : pkv_launch_prefill_bf16)(
+        p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv, stream);
+  if (cache->num_blocks > INT32_MAX) return PKV_ERR_ARG;  // block coordinates are 32-bit
+  return (f16 ? pkv_launch_prefill_tc_f16 : pkv_launch_prefill_tc_bf16)(
+      p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv, stream);
 }
 
 int paged_block_copy(const pkv_cache* cache, const int64_t* src_dst_pairs, int64_t num_pairs,

@@ -1,0 +1,505 @@
+// Paged causal prefill attention on the fifth-generation tensor cores
+// (tcgen05, accumulators in tensor memory), fp16 / bf16 pools.
+//
+// Same operation as prefill_mma_kernel ("vLLM and PagedAttention: Virtual
+// Memory for LLM Serving", opening paragraph; "Inside vLLM and TGI: Paging,
+// Versioned Schedulers and Operations", launch notes on chunked prefill):
+// sequence s holds L positions after its chunk of Q new queries was written;
+// query i sits at position L - Q + i and attends to positions 0 .. L - Q + i
+// through the block table.
+//
+// Work decomposition (this library's design): one CTA per (query tile, KV
+// head, sequence).  A query tile is 128 rows, each a (query, grouped head)
+// pair, so the G query heads sharing a KV head share every K/V tile.  Keys
+// stream in tiles of 128 positions.  Six warps with fixed roles:
+//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r): loads its
+//              S row from tensor memory, masks keys past its position, keeps
+//              the running maximum and sum, writes P (16-bit; bf16 as high
+//              and low parts) back over the S buffer, rescales its O row
+//              when needed, and finally
+//              normalises and stores O;
+//   warp 4     producer: 4-D TMA tile loads of K and V pages into a two-stage
+//              ring (128-byte swizzle); allocates the tensor memory;
+//   warp 5     MMA issuer (one thread): S = Q.K^T (A and B from shared
+//              memory, 128 x 128 x D) into one of two S buffers, then
+//              O += P.V (A = P from tensor memory, B = V from shared memory
+//              in MN-major form, 128 x D x 128); zeroes value rows past the
+//              last needed key before the last P.V.
+// S_j+1 is computed while the softmax works on S_j, and P.V of tile j-1 runs
+// meanwhile.  The running maximum is raised lazily: O and the sum are
+// rescaled only when a row's maximum grows by more than 2^8, so P stays
+// below 256 and most tiles skip the tensor-memory round trip of O.
+//
+// Tensor memory (512 columns): S0 at column 0, S1 at 128, O at 256.
+// Every wait is bounded; on a timeout the roles stop, the MMA issuer waits
+// for its MMAs to drain, and the tensor memory is released on every path.
+#pragma once
+
+#include <type_traits>
+
+#include "prefill.cuh"
+#include "tcgen05.cuh"
+
+namespace pkv {
+
+template <typename T, int D, int BS, int G>
+struct PrefillTcCfg {
+  static constexpr int kRows = 128;            // (query, head) rows = tensor-memory lanes
+  static constexpr int kQueries = kRows / G;   // queries per CTA
+  static constexpr int kKeys = 128;            // keys per tile
+  static constexpr int kHalves = D / 64;       // 128-byte column blocks
+  static constexpr int kHalfBytes = 128 * 128; // 128 rows x 128 B
+  static constexpr int kTileBytes = kHalves * kHalfBytes;
+  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kBoxRows = BS < 16 ? BS : 16;
+  static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
+  static constexpr int kProducerWarp = 4;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kThreads = 6 * 32;
+  static constexpr int kQOff = 0;
+  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kNumBars = 3 * kStages + 7;
+  static constexpr int kSlotOff = kBarOff + kNumBars * 8;
+  static constexpr int kAlign = 1024;
+  static constexpr int kSmemBytes = kAlign + kSlotOff + 16;
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  static constexpr uint32_t kIdescS = idesc_f16(kFmt, 128, kKeys, false);
+  static constexpr uint32_t kIdescPV = idesc_f16(kFmt, 128, D, true);
+  // bf16 P keeps 8 significant bits; split into high and low bf16 parts
+  // (two P.V MMAs) it keeps ~16, like the fp32 softmax it comes from.
+  static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+  static constexpr uint32_t kPLoCol = 64;  // P low part, in the same S buffer
+  static_assert(kBoxes <= 32, "one producer lane per box");
+  static_assert(kSmemBytes > 116 * 1024, "one CTA per SM: the tensor memory is not shared");
+  static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+template <typename T>
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi);
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__half>(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+template <>
+__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <typename T, int D, int BS, int G>
+__global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G>::kThreads, 1)
+prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv) {
+  using Cfg = PrefillTcCfg<T, D, BS, G>;
+  constexpr int NS = Cfg::kStages;
+  constexpr int KT = Cfg::kKeys;
+  constexpr int RB = Cfg::kBoxRows;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* smem = smem_raw + ((Cfg::kAlign - (smem_addr(smem_raw) & (Cfg::kAlign - 1))) &
+                                    (Cfg::kAlign - 1));
+  const uint32_t sbase = smem_addr(smem);
+
+  const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest tiles first
+  const int kvh = blockIdx.y;
+  const int s = blockIdx.z;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = p.num_heads;
+  T* out = static_cast<T*>(p.out);
+
+  const int q0 = p.starts[s];
+  const int q1 = p.starts[s + 1];
+  const int L = p.seq_lens[s];
+  if (q0 < 0 || q1 < q0 || q1 > p.total_queries) {  // cannot even locate the rows
+    if (tile == 0 && kvh == 0 && threadIdx.x == 0) set_error(p.err, PKV_DEV_SEQ_LEN);
+    return;
+  }
+  const int Q = q1 - q0;
+  const int qa = tile * Cfg::kQueries;
+  if (qa >= Q) return;
+  const int qend = min(Q, qa + Cfg::kQueries);
+  auto zero_rows = [&]() {
+    for (int e = threadIdx.x; e < (qend - qa) * G * D; e += Cfg::kThreads) {
+      const int qi = qa + e / (G * D);
+      const int rest = e % (G * D);
+      out[((int64_t)(q0 + qi) * H + kvh * G) * D + rest] = Elem<T>::from_f(0.f);
+    }
+  };
+  if (Q > L || Q > p.max_queries || L > p.max_blocks * BS) {
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SEQ_LEN);
+    zero_rows();
+    return;
+  }
+  const int first = L - Q;          // position of query 0
+  const int n_keys = first + qend;  // keys 0 .. n_keys-1 are visible to some row
+  const int nblk = (n_keys + BS - 1) / BS;
+  const int n_tiles = (n_keys + KT - 1) / KT;
+  const int32_t* trow = p.tables + (int64_t)s * p.max_blocks;
+  int bad = 0;
+  for (int i = threadIdx.x; i < nblk; i += Cfg::kThreads) {
+    const int e = trow[i];
+    bad |= (e < 0 || (int64_t)e >= p.num_blocks);
+  }
+  if (__syncthreads_or(bad)) {
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_TABLE_RANGE);
+    zero_rows();
+    return;
+  }
+
+  // ---- barriers, tensor memory, Q tile --------------------------------------
+  const uint32_t bar0 = sbase + Cfg::kBarOff;
+  auto k_full = [&](int st) { return bar0 + 8u * st; };
+  auto v_full = [&](int st) { return bar0 + 8u * (NS + st); };
+  auto kv_empty = [&](int st) { return bar0 + 8u * (2 * NS + st); };
+  auto s_full = [&](int b) { return bar0 + 8u * (3 * NS + b); };
+  auto p_full = [&](int b) { return bar0 + 8u * (3 * NS + 2 + b); };
+  const uint32_t o_done = bar0 + 8u * (3 * NS + 4);
+  const uint32_t drain = bar0 + 8u * (3 * NS + 5);
+  const uint32_t o_last = bar0 + 8u * (3 * NS + 6);  // the last P.V (single use)
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(k_full(st), 1);
+      mbar_init(v_full(st), 1);
+      mbar_init(kv_empty(st), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(p_full(b), Cfg::kRows);
+    }
+    mbar_init(o_done, 1);
+    mbar_init(drain, 1);
+    mbar_init(o_last, 1);
+    fence_mbar_init();
+  }
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Cfg::kSlotOff);
+  if (warp == Cfg::kProducerWarp) {
+    tmem_alloc(smem_addr(slot), Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  // Row r of the tile: query min(qa + r / G, Q - 1) (padding rows repeat the
+  // last query and are not stored), head kvh * G + r % G.  The softmax
+  // threads copy their Q rows into the 128-byte-swizzled operand layout.
+  const int r = threadIdx.x;
+  const int qi = min(qa + r / G, Q - 1);
+  if (warp < 4) {
+    const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
+                                                       ((int64_t)(q0 + qi) * H + kvh * G + r % G) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const int half = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + half * Cfg::kHalfBytes + r * 128 +
+                                ((cc ^ (r & 7)) << 4)) = qrow[c];
+    }
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  bool failed = false;
+
+  if (warp == Cfg::kProducerWarp) {
+    // ---- producer: K and V tiles ------------------------------------------
+    const uint64_t policy = policy_evict_last();
+    const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
+    int issued = 0;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j % NS;
+      if (j >= NS) {
+        const bool ok = mbar_wait(kv_empty(st), (uint32_t)(((j / NS) - 1) & 1));
+        if (__any_sync(kFullMask, !ok)) {
+          failed = true;
+          break;
+        }
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(k_full(st), Cfg::kTileBytes);
+        mbar_arrive_expect_tx(v_full(st), Cfg::kTileBytes);
+      }
+      __syncwarp();
+      const uint32_t kdst = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
+      const uint32_t vdst = kdst + Cfg::kTileBytes;
+      if (lane < Cfg::kBoxes) {
+        const int pos = j * KT + lane * RB;
+        // Boxes wholly past the last needed key read an out-of-range block:
+        // the copy fills them with zeros.
+        int pb = oob_block, row = 0;
+        if (pos < n_keys) {
+          pb = trow[pos / BS];
+          row = pos % BS;
+        }
+#pragma unroll
+        for (int h = 0; h < Cfg::kHalves; ++h) {
+          const uint32_t o = h * Cfg::kHalfBytes + lane * RB * 128;
+          tma_load_4d(kdst + o, &tmk, h * 64, row, kvh, pb, k_full(st), policy);
+          tma_load_4d(vdst + o, &tmv, h * 64, row, kvh, pb, v_full(st), policy);
+        }
+      }
+      issued = j + 1;
+    }
+    // Copies issued but possibly never consumed (another role stopped).
+    for (int j = issued - NS < 0 ? 0 : issued - NS; j < issued; ++j) {
+      mbar_wait(k_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
+      mbar_wait(v_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
+    }
+  } else if (warp == Cfg::kMmaWarp) {
+    // ---- MMA issuer -------------------------------------------------------
+    const uint32_t qbase = sbase + Cfg::kQOff;
+    auto pv = [&](int i) -> bool {
+      const int st = i % NS, sb = i & 1;
+      const bool ok = mbar_wait(p_full(sb), (uint32_t)((i >> 1) & 1)) &&
+                      mbar_wait(v_full(st), (uint32_t)((i / NS) & 1));
+      if (__any_sync(kFullMask, !ok)) return false;
+      const uint32_t vbase = sbase + Cfg::kRingOff + st * Cfg::kStageBytes + Cfg::kTileBytes;
+      const int valid = n_keys - i * KT;
+      if (valid < KT) {
+        // Value rows past the last needed key hold stale pool contents (0 * NaN
+        // would poison O): zero them.
+        unsigned char* vt = smem + (vbase - sbase);
+        for (int e = lane; e < (KT - valid) * Cfg::kHalves * 8; e += 32) {
+          const int row = valid + e / (Cfg::kHalves * 8);
+          const int rest = e % (Cfg::kHalves * 8);
+          *reinterpret_cast<uint4*>(vt + (rest >> 3) * Cfg::kHalfBytes + row * 128 +
+                                    (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+      tc_fence_after();
+      if (lane == 0) {
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          // MN-major V: 64-dim atoms kHalfBytes apart, 8-key groups 1024 B
+          // apart.  With one atom (D = 64) the atom stride is unused; 1024
+          // keeps every address inside the tile whichever field is read.
+          const uint64_t bdesc = smem_desc_sw128(
+              vbase + kk * 2048, Cfg::kHalves > 1 ? Cfg::kHalfBytes : 1024, 1024);
+          tc_mma_ts(tmem + Cfg::kOCol, tmem + sb * 128 + kk * 8, bdesc, Cfg::kIdescPV,
+                    (i > 0 || kk > 0) ? 1u : 0u);
+          if (Cfg::kSplitP)
+            tc_mma_ts(tmem + Cfg::kOCol, tmem + sb * 128 + Cfg::kPLoCol + kk * 8, bdesc,
+                      Cfg::kIdescPV, 1u);
+        }
+        tc_commit(o_done);
+        tc_commit(kv_empty(st));
+        if (i == n_tiles - 1) tc_commit(o_last);
+      }
+      __syncwarp();
+      return true;
+    };
+    bool ok = true;
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int st = j % NS, sb = j & 1;
+      ok = mbar_wait(k_full(st), (uint32_t)((j / NS) & 1));
+      if (__any_sync(kFullMask, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t kbase = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32;
+          tc_mma_ss(tmem + sb * 128, smem_desc_sw128(qbase + off, 16, 1024),
+                    smem_desc_sw128(kbase + off, 16, 1024), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(sb));
+      }
+      __syncwarp();
+      if (j >= 1) ok = pv(j - 1);
+    }
+    if (ok) ok = pv(n_tiles - 1);
+    failed = !ok;
+    // Every MMA issued has completed before the tensor memory is released.
+    if (lane == 0) tc_commit(drain);
+    __syncwarp();
+    mbar_wait(drain, 0);
+  } else {
+    // ---- softmax, row r ----------------------------------------------------
+    const int pos = first + qi;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      ok = mbar_wait(s_full(sb), (uint32_t)((j >> 1) & 1));
+      if (__any_sync(kFullMask, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float x[KT];
+      const int lim = pos - j * KT;  // keys c <= lim are visible
+#pragma unroll
+      for (int c4 = 0; c4 < KT / 32; ++c4) {
+        uint32_t w[32];
+        tmem_ld32(lane_base + sb * 128 + c4 * 32, w);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          x[c4 * 32 + i] = c4 * 32 + i <= lim ? __uint_as_float(w[i]) * p.qscale : -INFINITY;
+      }
+      float mx = x[0];
+#pragma unroll
+      for (int c = 1; c < KT; ++c) mx = fmaxf(mx, x[c]);
+      // Lazy maximum: raise it (and rescale O and l) only when the tile's
+      // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
+      // sees key 0 in tile 0, so m is finite from then on.
+      const bool raise = mx > m + 8.f;
+      if (j == 0) {
+        m = mx;
+      } else if (__any_sync(kFullMask, raise)) {
+        const float mnew = raise ? mx : m;
+        const float alpha = exp2f(m - mnew);
+        // P.V of tile j-1 is in O.  S_j done implies P.V of tile j-2 done
+        // (MMAs complete in issue order), so o_done is at most one phase
+        // behind and the parity wait is exact.
+        ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1));
+        if (__any_sync(kFullMask, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t w[32];
+          tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, w);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
+          tmem_st32(lane_base + Cfg::kOCol + c4 * 32, w);
+        }
+        l *= alpha;
+        m = mnew;
+      }
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < KT; ++c) {
+        x[c] = exp2f(x[c] - m);
+        sum += x[c];
+      }
+      l += sum;
+#pragma unroll
+      for (int h = 0; h < KT / 64; ++h) {
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) w[i] = pack_pair<T>(x[h * 64 + 2 * i], x[h * 64 + 2 * i + 1]);
+        tmem_st32(lane_base + sb * 128 + h * 32, w);
+        if (Cfg::kSplitP) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float a = x[h * 64 + 2 * i], b = x[h * 64 + 2 * i + 1];
+            w[i] = pack_pair<T>(a - __bfloat162float(__float2bfloat16_rn(a)),
+                                b - __bfloat162float(__float2bfloat16_rn(b)));
+          }
+          tmem_st32(lane_base + sb * 128 + Cfg::kPLoCol + h * 32, w);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(p_full(sb));
+    }
+    // ---- epilogue: O / l into the output rows that are real queries ---------
+    // o_done may trail by two phases here, which a parity wait cannot
+    // tell apart: the last P.V signals its own barrier.
+    if (ok) {
+      ok = mbar_wait(o_last, 0);
+      ok = !__any_sync(kFullMask, !ok);
+    }
+    failed = !ok;
+    if (ok) {
+      tc_fence_after();
+      const bool real = qa + r / G < qend;
+      const float inv = 1.f / l;
+      uint4* orow = reinterpret_cast<uint4*>(out + ((int64_t)(q0 + qi) * H + kvh * G + r % G) * D);
+#pragma unroll
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t w[32];
+        tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, w);
+        if (real) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint4 u;
+            u.x = pack_pair<T>(__uint_as_float(w[8 * v + 0]) * inv, __uint_as_float(w[8 * v + 1]) * inv);
+            u.y = pack_pair<T>(__uint_as_float(w[8 * v + 2]) * inv, __uint_as_float(w[8 * v + 3]) * inv);
+            u.z = pack_pair<T>(__uint_as_float(w[8 * v + 4]) * inv, __uint_as_float(w[8 * v + 5]) * inv);
+            u.w = pack_pair<T>(__uint_as_float(w[8 * v + 6]) * inv, __uint_as_float(w[8 * v + 7]) * inv);
+            orow[c4 * 4 + v] = u;
+          }
+        }
+      }
+    }
+  }
+
+  // ---- release the tensor memory ------------------------------------------
+  if (failed && lane == 0) set_error(p.err, PKV_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == Cfg::kProducerWarp) tmem_dealloc(tmem, Cfg::kTmemCols);
+}
+
+template <typename T, int D, int BS, int G>
+int launch_prefill_tc_cfg(const PrefillParams& p, int num_seqs, const CUtensorMap& mk,
+                          const CUtensorMap& mv, cudaStream_t stream) {
+  using Cfg = PrefillTcCfg<T, D, BS, G>;
+  auto kern = prefill_tc_kernel<T, D, BS, G>;
+  static std::atomic<uint64_t> ready{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
+  const uint64_t bit = 1ull << (dev & 63);
+  if (!(ready.load() & bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::kSmemBytes) != cudaSuccess)
+      return PKV_ERR_CUDA;
+    ready.fetch_or(bit);
+  }
+  dim3 grid((unsigned)((p.max_queries + Cfg::kQueries - 1) / Cfg::kQueries), (unsigned)p.kv_heads,
+            (unsigned)num_seqs);
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, mk, mv);
+  return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+template <typename T, int D, int BS>
+int launch_prefill_tc_g(const PrefillParams& p, int num_seqs, int group, const CUtensorMap& mk,
+                        const CUtensorMap& mv, cudaStream_t stream) {
+  switch (group) {
+    case 1: return launch_prefill_tc_cfg<T, D, BS, 1>(p, num_seqs, mk, mv, stream);
+    case 2: return launch_prefill_tc_cfg<T, D, BS, 2>(p, num_seqs, mk, mv, stream);
+    case 4: return launch_prefill_tc_cfg<T, D, BS, 4>(p, num_seqs, mk, mv, stream);
+    case 8: return launch_prefill_tc_cfg<T, D, BS, 8>(p, num_seqs, mk, mv, stream);
+  }
+  return PKV_ERR_GEOMETRY;
+}
+
+template <typename T>
+int launch_prefill_tc(const PrefillParams& p, int num_seqs, int head_dim, int block_size,
+                      int group, const CUtensorMap& mk, const CUtensorMap& mv,
+                      cudaStream_t stream) {
+  switch (head_dim * 1000 + block_size) {
+    case 64008: return launch_prefill_tc_g<T, 64, 8>(p, num_seqs, group, mk, mv, stream);
+    case 64016: return launch_prefill_tc_g<T, 64, 16>(p, num_seqs, group, mk, mv, stream);
+    case 64032: return launch_prefill_tc_g<T, 64, 32>(p, num_seqs, group, mk, mv, stream);
+    case 64064: return launch_prefill_tc_g<T, 64, 64>(p, num_seqs, group, mk, mv, stream);
+    case 128008: return launch_prefill_tc_g<T, 128, 8>(p, num_seqs, group, mk, mv, stream);
+    case 128016: return launch_prefill_tc_g<T, 128, 16>(p, num_seqs, group, mk, mv, stream);
+    case 128032: return launch_prefill_tc_g<T, 128, 32>(p, num_seqs, group, mk, mv, stream);
+    case 128064: return launch_prefill_tc_g<T, 128, 64>(p, num_seqs, group, mk, mv, stream);
+  }
+  return PKV_ERR_GEOMETRY;
+}
+
+}  // namespace pkv

@@ -17,6 +17,16 @@ pytestmark = pytest.mark.gpu
 TORCH = synth.TORCH_DTYPE
 
 
+@pytest.fixture(autouse=True, params=["tcgen05", "mma"])
+def kernel(request, monkeypatch):
+    """Every case on the tcgen05 kernel (default) and the mma.sync one."""
+    if request.param == "mma":
+        monkeypatch.setenv("PKV_PREFILL_KERNEL", "mma")
+    else:
+        monkeypatch.delenv("PKV_PREFILL_KERNEL", raising=False)
+    return request.param
+
+
 class PCase:
     """Scattered tables over a random pool; per sequence a cached prefix and a
     chunk of new queries (their keys already in the pool)."""
