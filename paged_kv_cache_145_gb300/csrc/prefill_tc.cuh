@@ -9,30 +9,33 @@
 // through the block table.
 //
 // Work decomposition (this library's design): one CTA per (query tile, KV
-// head, sequence).  A query tile is 128 rows, each a (query, grouped head)
-// pair, so the G query heads sharing a KV head share every K/V tile.  Keys
-// stream in tiles of 128 positions.  Six warps with fixed roles:
-//   warps 0-3  softmax: thread r owns row r (tensor-memory lane r): loads its
-//              S row from tensor memory, masks keys past its position, keeps
-//              the running maximum and sum, writes P (16-bit; bf16 as high
-//              and low parts) back over the S buffer, rescales its O row
-//              when needed, and finally
+// head, sequence).  A CTA holds two Q tiles, A and B, of 128 rows each; a
+// row is a (query, grouped head) pair, so the G query heads sharing a KV
+// head share every K/V tile.  Keys stream in tiles of 128 positions.  Ten
+// warps with fixed roles:
+//   warps 0-7  softmax: warp w serves Q tile w / 4; thread = one row =
+//              one tensor-memory lane: loads its S row from tensor memory,
+//              masks keys past its position, keeps the running maximum and
+//              sum, writes P (16-bit; bf16 as high and low parts) back over
+//              its S buffer, rescales its O row when needed, and finally
 //              normalises and stores O;
-//   warp 4     producer: 4-D TMA tile loads of K and V pages into a two-stage
-//              ring (128-byte swizzle); allocates the tensor memory;
-//   warp 5     MMA issuer (one thread): S = Q.K^T (A and B from shared
-//              memory, 128 x 128 x D) into one of two S buffers, then
-//              O += P.V (A = P from tensor memory, B = V from shared memory
-//              in MN-major form, 128 x D x 128); zeroes value rows past the
-//              last needed key before the last P.V.
-// S_j+1 is computed while the softmax works on S_j, and P.V of tile j-1 runs
-// meanwhile.  The running maximum is raised lazily: O and the sum are
-// rescaled only when a row's maximum grows by more than 2^8, so P stays
-// below 256 and most tiles skip the tensor-memory round trip of O.
+//   warp 8     producer: 4-D TMA tile loads of K and V pages into a ring
+//              (128-byte swizzle); allocates the tensor memory;
+//   warp 9     MMA issuer (one thread): S_t = Q_t.K^T (A and B from shared
+//              memory, 128 x 128 x D) and O_t += P_t.V (A = P_t from tensor
+//              memory, B = V from shared memory in MN-major form,
+//              128 x D x 128), in the order P.V_A(j-1), S_A(j), P.V_B(j-1),
+//              S_B(j): while one tile's softmax runs, the tensor core works
+//              on the other's; zeroes value rows past the last needed key
+//              before the last P.V.
+// The running maximum is raised lazily: O and the sum are rescaled only
+// when a row's maximum grows by more than 2^8, so P stays at or below 256
+// and most tiles skip the tensor-memory round trip of O.
 //
-// Tensor memory (512 columns): S0 at column 0, S1 at 128, O at 256.
-// Every wait is bounded; on a timeout the roles stop, the MMA issuer waits
-// for its MMAs to drain, and the tensor memory is released on every path.
+// Tensor memory (512 columns): S_A at column 0, S_B at 128, O_A at 256,
+// O_B at 256 + D.  Every wait is bounded; on a timeout the roles stop, the
+// MMA issuer waits for its MMAs to drain, and the tensor memory is released
+// on every path.
 #pragma once
 
 #include <type_traits>
@@ -44,28 +47,30 @@ namespace pkv {
 
 template <typename T, int D, int BS, int G>
 struct PrefillTcCfg {
-  static constexpr int kRows = 128;            // (query, head) rows = tensor-memory lanes
-  static constexpr int kQueries = kRows / G;   // queries per CTA
-  static constexpr int kKeys = 128;            // keys per tile
-  static constexpr int kHalves = D / 64;       // 128-byte column blocks
-  static constexpr int kHalfBytes = 128 * 128; // 128 rows x 128 B
+  static constexpr int kTileRows = 128;          // rows per Q tile = tensor-memory lanes
+  static constexpr int kRows = 2 * kTileRows;    // two Q tiles per CTA (A and B)
+  static constexpr int kQueries = kRows / G;     // queries per CTA
+  static constexpr int kKeys = 128;              // keys per K/V tile
+  static constexpr int kHalves = D / 64;         // 128-byte column blocks
+  static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B
   static constexpr int kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kStages = D == 64 ? 4 : 2;
+  static constexpr int kStages = D == 64 ? 3 : 2;
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
-  static constexpr int kProducerWarp = 4;
-  static constexpr int kMmaWarp = 5;
-  static constexpr int kThreads = 6 * 32;
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kSoftmaxWarps = 8;
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;
+  static constexpr int kThreads = 10 * 32;
+  static constexpr int kQOff = 0;                // Q tile t at t * kTileBytes
+  static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 3 * kStages + 7;
+  static constexpr int kNumBars = 3 * kStages + 6;
   static constexpr int kSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAlign = 1024;
   static constexpr int kSmemBytes = kAlign + kSlotOff + 16;
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 256;
+  static constexpr uint32_t kOCol = 256;         // O of tile t at kOCol + t * D
   static constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   static constexpr uint32_t kIdescS = idesc_f16(kFmt, 128, kKeys, false);
   static constexpr uint32_t kIdescPV = idesc_f16(kFmt, 128, D, true);
@@ -86,6 +91,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+
+// 2^x with the hardware approximation (flushes results below 2^-126 to 0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <typename T>
@@ -161,27 +173,25 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     return;
   }
 
-  // ---- barriers, tensor memory, Q tile --------------------------------------
+  // ---- barriers, tensor memory, Q tiles -------------------------------------
   const uint32_t bar0 = sbase + Cfg::kBarOff;
   auto k_full = [&](int st) { return bar0 + 8u * st; };
   auto v_full = [&](int st) { return bar0 + 8u * (NS + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (2 * NS + st); };
-  auto s_full = [&](int b) { return bar0 + 8u * (3 * NS + b); };
-  auto p_full = [&](int b) { return bar0 + 8u * (3 * NS + 2 + b); };
-  const uint32_t o_done = bar0 + 8u * (3 * NS + 4);
-  const uint32_t drain = bar0 + 8u * (3 * NS + 5);
-  const uint32_t o_last = bar0 + 8u * (3 * NS + 6);  // the last P.V (single use)
+  auto s_full = [&](int t) { return bar0 + 8u * (3 * NS + t); };  // S of Q tile t
+  auto p_full = [&](int t) { return bar0 + 8u * (3 * NS + 2 + t); };
+  const uint32_t drain = bar0 + 8u * (3 * NS + 4);
+  const uint32_t o_last = bar0 + 8u * (3 * NS + 5);  // the last P.V (single use)
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
       mbar_init(k_full(st), 1);
       mbar_init(v_full(st), 1);
       mbar_init(kv_empty(st), 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(s_full(b), 1);
-      mbar_init(p_full(b), Cfg::kRows);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(s_full(t), 1);
+      mbar_init(p_full(t), Cfg::kTileRows);
     }
-    mbar_init(o_done, 1);
     mbar_init(drain, 1);
     mbar_init(o_last, 1);
     fence_mbar_init();
@@ -191,19 +201,24 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     tmem_alloc(smem_addr(slot), Cfg::kTmemCols);
     tmem_relinquish();
   }
-  // Row r of the tile: query min(qa + r / G, Q - 1) (padding rows repeat the
-  // last query and are not stored), head kvh * G + r % G.  The softmax
-  // threads copy their Q rows into the 128-byte-swizzled operand layout.
-  const int r = threadIdx.x;
-  const int qi = min(qa + r / G, Q - 1);
-  if (warp < 4) {
+  // Softmax thread: Q tile t = warp / 4, row rr = (warp % 4) * 32 + lane of
+  // it (tensor-memory lane rr), CTA row R = t * 128 + rr: query
+  // min(qa + R / G, Q - 1) (padding rows repeat the last query and are not
+  // stored), head kvh * G + R % G.  It copies its Q row into the
+  // 128-byte-swizzled operand layout.
+  const int t = (warp >> 2) & 1;
+  const int rr = (warp & 3) * 32 + lane;
+  const int R = t * Cfg::kTileRows + rr;
+  const int qi = min(qa + R / G, Q - 1);
+  if (warp < Cfg::kSoftmaxWarps) {
     const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
-                                                       ((int64_t)(q0 + qi) * H + kvh * G + r % G) * D);
+                                                       ((int64_t)(q0 + qi) * H + kvh * G + R % G) * D);
+    unsigned char* qt = smem + Cfg::kQOff + t * Cfg::kTileBytes;
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const int half = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + half * Cfg::kHalfBytes + r * 128 +
-                                ((cc ^ (r & 7)) << 4)) = qrow[c];
+      *reinterpret_cast<uint4*>(qt + half * Cfg::kHalfBytes + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
+          qrow[c];
     }
     fence_proxy_async_smem();
   }
@@ -258,19 +273,61 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       mbar_wait(v_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
     }
   } else if (warp == Cfg::kMmaWarp) {
-    // ---- MMA issuer -------------------------------------------------------
-    const uint32_t qbase = sbase + Cfg::kQOff;
-    auto pv = [&](int i) -> bool {
-      const int st = i % NS, sb = i & 1;
-      const bool ok = mbar_wait(p_full(sb), (uint32_t)((i >> 1) & 1)) &&
-                      mbar_wait(v_full(st), (uint32_t)((i / NS) & 1));
-      if (__any_sync(kFullMask, !ok)) return false;
-      const uint32_t vbase = sbase + Cfg::kRingOff + st * Cfg::kStageBytes + Cfg::kTileBytes;
-      const int valid = n_keys - i * KT;
-      if (valid < KT) {
-        // Value rows past the last needed key hold stale pool contents (0 * NaN
-        // would poison O): zero them.
-        unsigned char* vt = smem + (vbase - sbase);
+    // ---- MMA issuer: S_A(0), S_B(0), then per tile j >= 1
+    //      P.V_A(j-1), S_A(j), P.V_B(j-1), S_B(j), and the last P.Vs.  Each
+    //      S_t(j) is issued after P.V_t(j-1), so when S_t(j) completes O_t
+    //      holds every tile before j (the softmax may rescale it at once).
+    auto wait_all = [&](uint32_t bar, int phase) {
+      const bool o = mbar_wait(bar, (uint32_t)(phase & 1));
+      return !__any_sync(kFullMask, !o);
+    };
+    auto issue_s = [&](int tt, int j) {
+      if (lane == 0) {
+        const uint32_t qb = sbase + Cfg::kQOff + tt * Cfg::kTileBytes;
+        const uint32_t kb = sbase + Cfg::kRingOff + (j % NS) * Cfg::kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32;
+          tc_mma_ss(tmem + tt * 128, smem_desc_sw128(qb + off, 16, 1024),
+                    smem_desc_sw128(kb + off, 16, 1024), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(s_full(tt));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int tt, int j) {
+      if (lane == 0) {
+        const uint32_t vb = sbase + Cfg::kRingOff + (j % NS) * Cfg::kStageBytes + Cfg::kTileBytes;
+        const uint32_t o = tmem + Cfg::kOCol + tt * D;
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          // MN-major V: 64-dim atoms kHalfBytes apart, 8-key groups 1024 B
+          // apart.  With one atom (D = 64) the atom stride is unused; 1024
+          // keeps every address inside the tile whichever field is read.
+          const uint64_t bdesc = smem_desc_sw128(
+              vb + kk * 2048, Cfg::kHalves > 1 ? Cfg::kHalfBytes : 1024, 1024);
+          tc_mma_ts(o, tmem + tt * 128 + kk * 8, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (Cfg::kSplitP)
+            tc_mma_ts(o, tmem + tt * 128 + Cfg::kPLoCol + kk * 8, bdesc, Cfg::kIdescPV, 1u);
+        }
+      }
+      __syncwarp();
+    };
+    bool ok = wait_all(k_full(0), 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+    }
+    for (int j = 1; j <= n_tiles && ok; ++j) {
+      const int jp = j - 1, stp = jp % NS;
+      ok = wait_all(p_full(0), jp) && wait_all(v_full(stp), jp / NS);
+      if (!ok) break;
+      if (jp == n_tiles - 1 && n_keys - jp * KT < KT) {
+        // Value rows past the last needed key hold stale pool contents
+        // (0 * NaN would poison O): zero them.
+        const int valid = n_keys - jp * KT;
+        unsigned char* vt = smem + Cfg::kRingOff + stp * Cfg::kStageBytes + Cfg::kTileBytes;
         for (int e = lane; e < (KT - valid) * Cfg::kHalves * 8; e += 32) {
           const int row = valid + e / (Cfg::kHalves * 8);
           const int rest = e % (Cfg::kHalves * 8);
@@ -281,82 +338,58 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         __syncwarp();
       }
       tc_fence_after();
-      if (lane == 0) {
-#pragma unroll
-        for (int kk = 0; kk < KT / 16; ++kk) {
-          // MN-major V: 64-dim atoms kHalfBytes apart, 8-key groups 1024 B
-          // apart.  With one atom (D = 64) the atom stride is unused; 1024
-          // keeps every address inside the tile whichever field is read.
-          const uint64_t bdesc = smem_desc_sw128(
-              vbase + kk * 2048, Cfg::kHalves > 1 ? Cfg::kHalfBytes : 1024, 1024);
-          tc_mma_ts(tmem + Cfg::kOCol, tmem + sb * 128 + kk * 8, bdesc, Cfg::kIdescPV,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-          if (Cfg::kSplitP)
-            tc_mma_ts(tmem + Cfg::kOCol, tmem + sb * 128 + Cfg::kPLoCol + kk * 8, bdesc,
-                      Cfg::kIdescPV, 1u);
-        }
-        tc_commit(o_done);
-        tc_commit(kv_empty(st));
-        if (i == n_tiles - 1) tc_commit(o_last);
+      issue_pv(0, jp);
+      if (j < n_tiles) {
+        ok = wait_all(k_full(j % NS), j / NS);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(0, j);
       }
-      __syncwarp();
-      return true;
-    };
-    bool ok = true;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      const int st = j % NS, sb = j & 1;
-      ok = mbar_wait(k_full(st), (uint32_t)((j / NS) & 1));
-      if (__any_sync(kFullMask, !ok)) {
-        ok = false;
-        break;
-      }
+      ok = wait_all(p_full(1), jp);
+      if (!ok) break;
       tc_fence_after();
-      if (lane == 0) {
-        const uint32_t kbase = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32;
-          tc_mma_ss(tmem + sb * 128, smem_desc_sw128(qbase + off, 16, 1024),
-                    smem_desc_sw128(kbase + off, 16, 1024), Cfg::kIdescS, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(s_full(sb));
-      }
-      __syncwarp();
-      if (j >= 1) ok = pv(j - 1);
+      issue_pv(1, jp);
+      if (lane == 0) tc_commit(kv_empty(stp));
+      if (j < n_tiles) issue_s(1, j);
     }
-    if (ok) ok = pv(n_tiles - 1);
+    if (ok && lane == 0) tc_commit(o_last);
     failed = !ok;
     // Every MMA issued has completed before the tensor memory is released.
     if (lane == 0) tc_commit(drain);
     __syncwarp();
     mbar_wait(drain, 0);
   } else {
-    // ---- softmax, row r ----------------------------------------------------
+    // ---- softmax, row rr of Q tile t ----------------------------------------
     const int pos = first + qi;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t scol = t * 128, ocol = Cfg::kOCol + t * D;
+    const float qscale = p.qscale;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
-      const int sb = j & 1;
-      ok = mbar_wait(s_full(sb), (uint32_t)((j >> 1) & 1));
+      ok = mbar_wait(s_full(t), (uint32_t)(j & 1));
       if (__any_sync(kFullMask, !ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      float x[KT];
-      const int lim = pos - j * KT;  // keys c <= lim are visible
+      float x[KT];  // raw scores; keys past this row's position are -inf
 #pragma unroll
       for (int c4 = 0; c4 < KT / 32; ++c4) {
         uint32_t w[32];
-        tmem_ld32(lane_base + sb * 128 + c4 * 32, w);
+        tmem_ld32(lane_base + scol + c4 * 32, w);
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          x[c4 * 32 + i] = c4 * 32 + i <= lim ? __uint_as_float(w[i]) * p.qscale : -INFINITY;
+        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(w[i]);
+      }
+      const int lim = pos - j * KT;  // keys c <= lim are visible
+      if (__any_sync(kFullMask, lim < KT - 1)) {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) x[c] = c <= lim ? x[c] : -INFINITY;
       }
       float mx = x[0];
 #pragma unroll
       for (int c = 1; c < KT; ++c) mx = fmaxf(mx, x[c]);
+      mx *= qscale;  // the scale is positive
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
       // sees key 0 in tile 0, so m is finite from then on.
@@ -365,56 +398,54 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         m = mx;
       } else if (__any_sync(kFullMask, raise)) {
         const float mnew = raise ? mx : m;
-        const float alpha = exp2f(m - mnew);
-        // P.V of tile j-1 is in O.  S_j done implies P.V of tile j-2 done
-        // (MMAs complete in issue order), so o_done is at most one phase
-        // behind and the parity wait is exact.
-        ok = mbar_wait(o_done, (uint32_t)((j - 1) & 1));
-        if (__any_sync(kFullMask, !ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
+        const float alpha = ex2(m - mnew);
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
           uint32_t w[32];
-          tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, w);
+          tmem_ld32(lane_base + ocol + c4 * 32, w);
 #pragma unroll
           for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-          tmem_st32(lane_base + Cfg::kOCol + c4 * 32, w);
+          tmem_st32(lane_base + ocol + c4 * 32, w);
         }
         l *= alpha;
         m = mnew;
       }
+      const float nm = -m;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < KT; ++c) {
-        x[c] = exp2f(x[c] - m);
+        x[c] = ex2(fmaf(x[c], qscale, nm));
         sum += x[c];
       }
       l += sum;
 #pragma unroll
       for (int h = 0; h < KT / 64; ++h) {
         uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) w[i] = pack_pair<T>(x[h * 64 + 2 * i], x[h * 64 + 2 * i + 1]);
-        tmem_st32(lane_base + sb * 128 + h * 32, w);
         if (Cfg::kSplitP) {
+          // High part: the upper 16 bits of each float (truncated bf16);
+          // low part: the exact remainder rounded to bf16.
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            w[i] = __byte_perm(__float_as_uint(x[h * 64 + 2 * i]),
+                               __float_as_uint(x[h * 64 + 2 * i + 1]), 0x7632);
+          tmem_st32(lane_base + scol + h * 32, w);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float a = x[h * 64 + 2 * i], b = x[h * 64 + 2 * i + 1];
-            w[i] = pack_pair<T>(a - __bfloat162float(__float2bfloat16_rn(a)),
-                                b - __bfloat162float(__float2bfloat16_rn(b)));
+            w[i] = pack_pair<T>(a - __uint_as_float(__float_as_uint(a) & 0xFFFF0000u),
+                                b - __uint_as_float(__float_as_uint(b) & 0xFFFF0000u));
           }
-          tmem_st32(lane_base + sb * 128 + Cfg::kPLoCol + h * 32, w);
+          tmem_st32(lane_base + scol + Cfg::kPLoCol + h * 32, w);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) w[i] = pack_pair<T>(x[h * 64 + 2 * i], x[h * 64 + 2 * i + 1]);
+          tmem_st32(lane_base + scol + h * 32, w);
         }
       }
       tc_fence_before();
-      mbar_arrive(p_full(sb));
+      mbar_arrive(p_full(t));
     }
     // ---- epilogue: O / l into the output rows that are real queries ---------
-    // o_done may trail by two phases here, which a parity wait cannot
-    // tell apart: the last P.V signals its own barrier.
     if (ok) {
       ok = mbar_wait(o_last, 0);
       ok = !__any_sync(kFullMask, !ok);
@@ -422,13 +453,13 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     failed = !ok;
     if (ok) {
       tc_fence_after();
-      const bool real = qa + r / G < qend;
+      const bool real = qa + R / G < qend;
       const float inv = 1.f / l;
-      uint4* orow = reinterpret_cast<uint4*>(out + ((int64_t)(q0 + qi) * H + kvh * G + r % G) * D);
+      uint4* orow = reinterpret_cast<uint4*>(out + ((int64_t)(q0 + qi) * H + kvh * G + R % G) * D);
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t w[32];
-        tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, w);
+        tmem_ld32(lane_base + ocol + c4 * 32, w);
         if (real) {
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
