@@ -77,8 +77,8 @@ struct PrefillTcCfg {
   // bf16 P keeps 8 significant bits; split into high and low bf16 parts
   // (two P.V MMAs) it keeps ~16, like the fp32 softmax it comes from.
   static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-  static constexpr uint32_t kPLoCol = 64;  // P low part, in the same S buffer
   static_assert(kBoxes <= 32, "one producer lane per box");
+  static_assert(kKeys == 128, "the softmax's P layout assumes 128-key tiles");
   static_assert(kSmemBytes > 116 * 1024, "one CTA per SM: the tensor memory is not shared");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -306,9 +306,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           // keeps every address inside the tile whichever field is read.
           const uint64_t bdesc = smem_desc_sw128(
               vb + kk * 2048, Cfg::kHalves > 1 ? Cfg::kHalfBytes : 1024, 1024);
-          tc_mma_ts(o, tmem + tt * 128 + kk * 8, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          if (Cfg::kSplitP)
-            tc_mma_ts(o, tmem + tt * 128 + Cfg::kPLoCol + kk * 8, bdesc, Cfg::kIdescPV, 1u);
+          // P of keys 16kk .. 16kk+15: columns 8kk .. 8kk+7, low part 64 further.
+          const uint32_t pa = tmem + tt * 128 + 8 * kk;
+          tc_mma_ts(o, pa, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (Cfg::kSplitP) tc_mma_ts(o, pa + 64, bdesc, Cfg::kIdescPV, 1u);
         }
       }
       __syncwarp();
@@ -373,73 +374,80 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         break;
       }
       tc_fence_after();
-      float x[KT];  // raw scores; keys past this row's position are -inf
-#pragma unroll
-      for (int c4 = 0; c4 < KT / 32; ++c4) {
-        uint32_t w[32];
-        tmem_ld32(lane_base + scol + c4 * 32, w);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) x[c4 * 32 + i] = __uint_as_float(w[i]);
-      }
+      // The S row (128 scores) in one tensor-memory round trip.  Keys past
+      // this row's position count as -inf; the mask is applied only on
+      // diagonal tiles.
+      uint32_t w[KT];
+      tmem_ld128(lane_base + scol, w);
       const int lim = pos - j * KT;  // keys c <= lim are visible
       if (__any_sync(kFullMask, lim < KT - 1)) {
 #pragma unroll
-        for (int c = 0; c < KT; ++c) x[c] = c <= lim ? x[c] : -INFINITY;
+        for (int c = 0; c < KT; ++c)
+          if (c > lim) w[c] = __float_as_uint(-INFINITY);
       }
-      float mx = x[0];
+      float mx = __uint_as_float(w[0]);
 #pragma unroll
-      for (int c = 1; c < KT; ++c) mx = fmaxf(mx, x[c]);
+      for (int c = 1; c < KT; ++c) mx = fmaxf(mx, __uint_as_float(w[c]));
       mx *= qscale;  // the scale is positive
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
       // sees key 0 in tile 0, so m is finite from then on.
-      const bool raise = mx > m + 8.f;
+      // O is rescaled after P is stored (the scores are dead by then), still
+      // before the P.V that adds this tile.
+      bool rescale = false;
+      float alpha = 1.f;
       if (j == 0) {
         m = mx;
-      } else if (__any_sync(kFullMask, raise)) {
-        const float mnew = raise ? mx : m;
-        const float alpha = ex2(m - mnew);
-#pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) {
-          uint32_t w[32];
-          tmem_ld32(lane_base + ocol + c4 * 32, w);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * alpha);
-          tmem_st32(lane_base + ocol + c4 * 32, w);
+      } else {
+        const bool raise = mx > m + 8.f;
+        rescale = __any_sync(kFullMask, raise);
+        if (raise) {
+          alpha = ex2(m - mx);
+          l *= alpha;
+          m = mx;
         }
-        l *= alpha;
-        m = mnew;
       }
       const float nm = -m;
       float sum = 0.f;
 #pragma unroll
       for (int c = 0; c < KT; ++c) {
-        x[c] = ex2(fmaf(x[c], qscale, nm));
-        sum += x[c];
+        const float x = ex2(fmaf(__uint_as_float(w[c]), qscale, nm));
+        w[c] = __float_as_uint(x);
+        sum += x;
       }
       l += sum;
+      // P over S: keys 2c, 2c+1 in column c (high part, or the only one);
+      // the bf16 low part of the same keys in column 64 + c.  Stored in two
+      // halves of 64 keys.
+      if (Cfg::kSplitP) {
 #pragma unroll
-      for (int h = 0; h < KT / 64; ++h) {
-        uint32_t w[32];
-        if (Cfg::kSplitP) {
-          // High part: the upper 16 bits of each float (truncated bf16);
-          // low part: the exact remainder rounded to bf16.
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            w[i] = __byte_perm(__float_as_uint(x[h * 64 + 2 * i]),
-                               __float_as_uint(x[h * 64 + 2 * i + 1]), 0x7632);
-          tmem_st32(lane_base + scol + h * 32, w);
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[64];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const float a = x[h * 64 + 2 * i], b = x[h * 64 + 2 * i + 1];
-            w[i] = pack_pair<T>(a - __uint_as_float(__float_as_uint(a) & 0xFFFF0000u),
-                                b - __uint_as_float(__float_as_uint(b) & 0xFFFF0000u));
+            const uint32_t a = w[64 * h + 2 * i], b = w[64 * h + 2 * i + 1];
+            pk[i] = __byte_perm(a, b, 0x7632);  // upper halves: truncated bf16
+            pk[32 + i] = pack_pair<T>(__uint_as_float(a) - __uint_as_float(a & 0xFFFF0000u),
+                                      __uint_as_float(b) - __uint_as_float(b & 0xFFFF0000u));
           }
-          tmem_st32(lane_base + scol + Cfg::kPLoCol + h * 32, w);
-        } else {
+          tmem_st2x32_nowait(lane_base + scol + 32 * h, lane_base + scol + 64 + 32 * h, pk);
+        }
+      } else {
+        uint32_t pk[64];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) w[i] = pack_pair<T>(x[h * 64 + 2 * i], x[h * 64 + 2 * i + 1]);
-          tmem_st32(lane_base + scol + h * 32, w);
+        for (int c = 0; c < KT / 2; ++c)
+          pk[c] = pack_pair<T>(__uint_as_float(w[2 * c]), __uint_as_float(w[2 * c + 1]));
+        tmem_st2x32_nowait(lane_base + scol, lane_base + scol + 32, pk);
+      }
+      tmem_wait_st();
+      if (rescale) {
+#pragma unroll 1
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + ocol + c4 * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + ocol + c4 * 32, o);
         }
       }
       tc_fence_before();
