@@ -93,6 +93,13 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Largest of three.
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 // 2^x with the hardware approximation (flushes results below 2^-126 to 0).
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -385,9 +392,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         for (int c = 0; c < KT; ++c)
           if (c > lim) w[c] = __float_as_uint(-INFINITY);
       }
-      float mx = __uint_as_float(w[0]);
+      float mx = -INFINITY;
 #pragma unroll
-      for (int c = 1; c < KT; ++c) mx = fmaxf(mx, __uint_as_float(w[c]));
+      for (int c = 0; c < KT; c += 2) mx = max3(mx, __uint_as_float(w[c]), __uint_as_float(w[c + 1]));
       mx *= qscale;  // the scale is positive
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
@@ -407,15 +414,20 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           m = mx;
         }
       }
-      const float nm = -m;
-      float sum = 0.f;
+      // Pairs of scores through the packed fp32 pipe: 2^(s * scale - m) and
+      // the running sum.
+      const float2 qs2 = make_float2(qscale, qscale), nm2 = make_float2(-m, -m);
+      float2 sum2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < KT; ++c) {
-        const float x = ex2(fmaf(__uint_as_float(w[c]), qscale, nm));
-        w[c] = __float_as_uint(x);
-        sum += x;
+      for (int c = 0; c < KT; c += 2) {
+        const float2 a = __ffma2_rn(make_float2(__uint_as_float(w[c]), __uint_as_float(w[c + 1])),
+                                    qs2, nm2);
+        const float2 e = make_float2(ex2(a.x), ex2(a.y));
+        w[c] = __float_as_uint(e.x);
+        w[c + 1] = __float_as_uint(e.y);
+        sum2 = __fadd2_rn(sum2, e);
       }
-      l += sum;
+      l += sum2.x + sum2.y;
       // P over S: keys 2c, 2c+1 in column c (high part, or the only one);
       // the bf16 low part of the same keys in column 64 + c.  Stored in two
       // halves of 64 keys.
@@ -427,8 +439,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           for (int i = 0; i < 32; ++i) {
             const uint32_t a = w[64 * h + 2 * i], b = w[64 * h + 2 * i + 1];
             pk[i] = __byte_perm(a, b, 0x7632);  // upper halves: truncated bf16
-            pk[32 + i] = pack_pair<T>(__uint_as_float(a) - __uint_as_float(a & 0xFFFF0000u),
-                                      __uint_as_float(b) - __uint_as_float(b & 0xFFFF0000u));
+            // exact remainders p - trunc(p), rounded to bf16
+            const float2 r = __ffma2_rn(
+                make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
+                make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
+            pk[32 + i] = pack_pair<T>(r.x, r.y);
           }
           tmem_st2x32_nowait(lane_base + scol + 32 * h, lane_base + scol + 64 + 32 * h, pk);
         }
