@@ -643,29 +643,37 @@ def run_prefill(args):
     scale = 1.0 / math.sqrt(D)
     stream = torch.cuda.current_stream()
 
-    def step(mid=None):
-        pkv.paged_kv_write(cache, k, v, sl)
-        if mid is not None:
-            mid.record(stream)
+    def attend():
         pkv.paged_attention_prefill(cache, q, starts, tab, ln, scale, chunk, out=out)
+
+    def step():
+        pkv.paged_kv_write(cache, k, v, sl)
+        attend()
+
+    def span(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        e1.record(stream)
+        return e0, e1
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     assert pkv.paged_get_device_error() == 0
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # Timed region: K steps back to back, then K attention launches alone
+    # (the roofline's per-launch time), one event pair each.
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
-    for a, m_, z in evs:
-        a.record(stream)
-        step(m_)
-        z.record(stream)
+    steps_ev = span(step)
+    attn_ev = span(attend)
     torch.cuda.synchronize()
     clocks = sampler.stop()
     assert pkv.paged_get_device_error() == 0
-    step_s = evs[0][0].elapsed_time(evs[-1][2]) / 1e3 / args.steps
-    attn_s = statistics.fmean(m_.elapsed_time(z) for _, m_, z in evs) / 1e3
+    step_s = steps_ev[0].elapsed_time(steps_ev[1]) / 1e3 / args.steps
+    attn_s = attn_ev[0].elapsed_time(attn_ev[1]) / 1e3 / args.steps
     # Algorithmic FLOPs: QK^T and PV, 2 * D each, per (query, head, visible key).
     visible = S * sum(prefix + i + 1 for i in range(chunk))
     flops = 4 * D * H * visible
@@ -684,9 +692,12 @@ def run_prefill(args):
         "prefill_tokens_per_s": round(T / step_s, 1),
         "roofline": {"bound": "tensor", "achieved": round(flops / attn_s / 1e12, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(flops / attn_s / 1e12 / peak, 4), "traffic": None,
-                     "kernel": "prefill_mma_kernel (mma.sync m16n8k16)", "peak_source": kind,
+                     "kernel": ("prefill_mma_kernel (mma.sync m16n8k16)"
+                                if os.environ.get("PKV_PREFILL_KERNEL") == "mma" else
+                                "prefill_tc_kernel (tcgen05.mma, TMEM accumulators)"),
+                     "peak_source": kind,
                      "attention_us": round(attn_s * 1e6, 2)},
-        "clocks": clocks, "gpu_launches": 2 * args.steps,
+        "clocks": clocks, "gpu_launches": 3 * args.steps,
     }
     print(json.dumps(line), flush=True)
 

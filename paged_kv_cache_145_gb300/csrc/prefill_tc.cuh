@@ -392,9 +392,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         for (int c = 0; c < KT; ++c)
           if (c > lim) w[c] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      // Row maximum: four independent chains of three-input maxima.
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int c = 0; c < KT; c += 2) mx = max3(mx, __uint_as_float(w[c]), __uint_as_float(w[c + 1]));
+      for (int c = 0; c < KT; c += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mq[u] = max3(mq[u], __uint_as_float(w[c + 2 * u]), __uint_as_float(w[c + 2 * u + 1]));
+      float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
       mx *= qscale;  // the scale is positive
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
@@ -417,7 +422,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       // Pairs of scores through the packed fp32 pipe: 2^(s * scale - m) and
       // the running sum.
       const float2 qs2 = make_float2(qscale, qscale), nm2 = make_float2(-m, -m);
-      float2 sum2 = make_float2(0.f, 0.f);
+      float2 sum2[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < KT; c += 2) {
         const float2 a = __ffma2_rn(make_float2(__uint_as_float(w[c]), __uint_as_float(w[c + 1])),
@@ -425,9 +431,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         const float2 e = make_float2(ex2(a.x), ex2(a.y));
         w[c] = __float_as_uint(e.x);
         w[c + 1] = __float_as_uint(e.y);
-        sum2 = __fadd2_rn(sum2, e);
+        sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
       }
-      l += sum2.x + sum2.y;
+      const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
+      const float2 st = __fadd2_rn(s01, s23);
+      l += st.x + st.y;
       // P over S: keys 2c, 2c+1 in column c (high part, or the only one);
       // the bf16 low part of the same keys in column 64 + c.  Stored in two
       // halves of 64 keys.
