@@ -21,7 +21,7 @@
 //              normalises and stores O;
 //   warp 8     producer: 4-D TMA tile loads of K and V pages into a ring
 //              (128-byte swizzle); allocates the tensor memory;
-//   warp 9     MMA issuer (one thread): S_t = Q_t.K^T (A and B from shared
+//   warps 9,10 MMA issuers (one thread each, Q tile A and B): S_t = Q_t.K^T (A and B from shared
 //              memory, 128 x 128 x D) and O_t += P_t.V (A = P_t from tensor
 //              memory, B = V from shared memory in MN-major form,
 //              128 x D x 128), in the order P.V_A(j-1), S_A(j), P.V_B(j-1),
@@ -50,27 +50,32 @@ struct PrefillTcCfg {
   static constexpr int kTileRows = 128;          // rows per Q tile = tensor-memory lanes
   static constexpr int kRows = 2 * kTileRows;    // two Q tiles per CTA (A and B)
   static constexpr int kQueries = kRows / G;     // queries per CTA
-  static constexpr int kKeys = 128;              // keys per K/V tile
+  static constexpr int kKeys = 64;               // keys per K/V tile
   static constexpr int kHalves = D / 64;         // 128-byte column blocks
   static constexpr int kHalfBytes = 128 * 128;   // 128 rows x 128 B
-  static constexpr int kTileBytes = kHalves * kHalfBytes;
-  static constexpr int kStages = D == 64 ? 3 : 2;
+  static constexpr int kTileBytes = kHalves * kHalfBytes;     // one Q tile (128 rows)
+  static constexpr int kKvHalfBytes = kKeys * 128;               // 64 key rows x 128 B
+  static constexpr int kKvBytes = kHalves * kKvHalfBytes;        // one K or V tile
+  static constexpr int kStages = D == 64 ? 6 : 4;
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
   static constexpr int kSoftmaxWarps = 8;
   static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;
-  static constexpr int kThreads = 10 * 32;
+  static constexpr int kMmaWarp = 9;             // warps 9 and 10: MMA issuers of Q tiles A, B
+  static constexpr int kThreads = 11 * 32;
   static constexpr int kQOff = 0;                // Q tile t at t * kTileBytes
   static constexpr int kRingOff = 2 * kTileBytes;
-  static constexpr int kStageBytes = 2 * kTileBytes;  // K then V
+  static constexpr int kStageBytes = 2 * kKvBytes;  // K then V
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 3 * kStages + 6;
+  static constexpr int kNumBars = 3 * kStages + 12;
   static constexpr int kSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAlign = 1024;
   static constexpr int kSmemBytes = kAlign + kSlotOff + 16;
+  // Tensor memory per Q tile t (base t * 256): S at +0 (64 columns), P at
+  // +64 (keys 2c, 2c+1 in column c; bf16 low part in 32 + c), O at +128.
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kOCol = 256;         // O of tile t at kOCol + t * D
+  static constexpr uint32_t kTileCols = 256;
+  static constexpr uint32_t kPCol = 64, kOCol = 128;
   static constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
   static constexpr uint32_t kIdescS = idesc_f16(kFmt, 128, kKeys, false);
   static constexpr uint32_t kIdescPV = idesc_f16(kFmt, 128, D, true);
@@ -78,8 +83,9 @@ struct PrefillTcCfg {
   // (two P.V MMAs) it keeps ~16, like the fp32 softmax it comes from.
   static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   static_assert(kBoxes <= 32, "one producer lane per box");
-  static_assert(kKeys == 128, "the softmax's P layout assumes 128-key tiles");
+  static_assert(kKeys == 64, "the softmax's P layout assumes 64-key tiles");
   static_assert(kSmemBytes > 116 * 1024, "one CTA per SM: the tensor memory is not shared");
+  static_assert(kOCol + D <= kTileCols, "tensor memory per Q tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
 
@@ -185,22 +191,27 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   auto k_full = [&](int st) { return bar0 + 8u * st; };
   auto v_full = [&](int st) { return bar0 + 8u * (NS + st); };
   auto kv_empty = [&](int st) { return bar0 + 8u * (2 * NS + st); };
-  auto s_full = [&](int t) { return bar0 + 8u * (3 * NS + t); };  // S of Q tile t
-  auto p_full = [&](int t) { return bar0 + 8u * (3 * NS + 2 + t); };
-  const uint32_t drain = bar0 + 8u * (3 * NS + 4);
-  const uint32_t o_last = bar0 + 8u * (3 * NS + 5);  // the last P.V (single use)
+  // Per Q tile t: S ready, S read (free), P written, P.V done (P free).
+  auto s_full = [&](int t) { return bar0 + 8u * (3 * NS + t); };
+  auto s_free = [&](int t) { return bar0 + 8u * (3 * NS + 2 + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (3 * NS + 4 + t); };
+  auto p_free = [&](int t) { return bar0 + 8u * (3 * NS + 6 + t); };
+  auto drain = [&](int t) { return bar0 + 8u * (3 * NS + 8 + t); };
+  auto o_last = [&](int t) { return bar0 + 8u * (3 * NS + 10 + t); };  // last P.V (single use)
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
       mbar_init(k_full(st), 1);
       mbar_init(v_full(st), 1);
-      mbar_init(kv_empty(st), 1);
+      mbar_init(kv_empty(st), 2);  // both Q tiles' P.V
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(s_full(t), 1);
+      mbar_init(s_free(t), Cfg::kTileRows);
       mbar_init(p_full(t), Cfg::kTileRows);
+      mbar_init(p_free(t), 1);
+      mbar_init(drain(t), 1);
+      mbar_init(o_last(t), 1);
     }
-    mbar_init(drain, 1);
-    mbar_init(o_last, 1);
     fence_mbar_init();
   }
   uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Cfg::kSlotOff);
@@ -250,12 +261,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         }
       }
       if (lane == 0) {
-        mbar_arrive_expect_tx(k_full(st), Cfg::kTileBytes);
-        mbar_arrive_expect_tx(v_full(st), Cfg::kTileBytes);
+        mbar_arrive_expect_tx(k_full(st), Cfg::kKvBytes);
+        mbar_arrive_expect_tx(v_full(st), Cfg::kKvBytes);
       }
       __syncwarp();
       const uint32_t kdst = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
-      const uint32_t vdst = kdst + Cfg::kTileBytes;
+      const uint32_t vdst = kdst + Cfg::kKvBytes;
       if (lane < Cfg::kBoxes) {
         const int pos = j * KT + lane * RB;
         // Boxes wholly past the last needed key read an out-of-range block:
@@ -267,7 +278,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         }
 #pragma unroll
         for (int h = 0; h < Cfg::kHalves; ++h) {
-          const uint32_t o = h * Cfg::kHalfBytes + lane * RB * 128;
+          const uint32_t o = h * Cfg::kKvHalfBytes + lane * RB * 128;
           tma_load_4d(kdst + o, &tmk, h * 64, row, kvh, pb, k_full(st), policy);
           tma_load_4d(vdst + o, &tmv, h * 64, row, kvh, pb, v_full(st), policy);
         }
@@ -279,11 +290,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       mbar_wait(k_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
       mbar_wait(v_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
     }
-  } else if (warp == Cfg::kMmaWarp) {
-    // ---- MMA issuer: S_A(0), S_B(0), then per tile j >= 1
-    //      P.V_A(j-1), S_A(j), P.V_B(j-1), S_B(j), and the last P.Vs.  Each
-    //      S_t(j) is issued after P.V_t(j-1), so when S_t(j) completes O_t
-    //      holds every tile before j (the softmax may rescale it at once).
+  } else if (warp >= Cfg::kMmaWarp) {
+    // ---- MMA issuers, one per Q tile t: S_t(0); then per K/V tile j:
+    //      S_t(j+1) once the softmax has read S_t(j), and P.V_t(j) once
+    //      P_t(j) is written.  The next S is computed while the softmax works
+    //      on the current one; P has its own columns, so only the next P
+    //      write waits for a P.V.  Separate issuers keep one tile's waits
+    //      from holding up the other's MMAs (commits track each thread's
+    //      own MMAs).
     auto wait_all = [&](uint32_t bar, int phase) {
       const bool o = mbar_wait(bar, (uint32_t)(phase & 1));
       return !__any_sync(kFullMask, !o);
@@ -294,9 +308,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         const uint32_t kb = sbase + Cfg::kRingOff + (j % NS) * Cfg::kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32;
-          tc_mma_ss(tmem + tt * 128, smem_desc_sw128(qb + off, 16, 1024),
-                    smem_desc_sw128(kb + off, 16, 1024), Cfg::kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t qo = (kk >> 2) * Cfg::kHalfBytes + (kk & 3) * 32;
+          const uint32_t ko = (kk >> 2) * Cfg::kKvHalfBytes + (kk & 3) * 32;
+          tc_mma_ss(tmem + tt * Cfg::kTileCols, smem_desc_sw128(qb + qo, 16, 1024),
+                    smem_desc_sw128(kb + ko, 16, 1024), Cfg::kIdescS, kk > 0 ? 1u : 0u);
         }
         tc_commit(s_full(tt));
       }
@@ -304,73 +319,71 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     };
     auto issue_pv = [&](int tt, int j) {
       if (lane == 0) {
-        const uint32_t vb = sbase + Cfg::kRingOff + (j % NS) * Cfg::kStageBytes + Cfg::kTileBytes;
-        const uint32_t o = tmem + Cfg::kOCol + tt * D;
+        const uint32_t vb = sbase + Cfg::kRingOff + (j % NS) * Cfg::kStageBytes + Cfg::kKvBytes;
+        const uint32_t base = tmem + tt * Cfg::kTileCols;
 #pragma unroll
         for (int kk = 0; kk < KT / 16; ++kk) {
-          // MN-major V: 64-dim atoms kHalfBytes apart, 8-key groups 1024 B
+          // MN-major V: 64-dim atoms kKvHalfBytes apart, 8-key groups 1024 B
           // apart.  With one atom (D = 64) the atom stride is unused; 1024
           // keeps every address inside the tile whichever field is read.
           const uint64_t bdesc = smem_desc_sw128(
-              vb + kk * 2048, Cfg::kHalves > 1 ? Cfg::kHalfBytes : 1024, 1024);
-          // P of keys 16kk .. 16kk+15: columns 8kk .. 8kk+7, low part 64 further.
-          const uint32_t pa = tmem + tt * 128 + 8 * kk;
-          tc_mma_ts(o, pa, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          if (Cfg::kSplitP) tc_mma_ts(o, pa + 64, bdesc, Cfg::kIdescPV, 1u);
+              vb + kk * 2048, Cfg::kHalves > 1 ? Cfg::kKvHalfBytes : 1024, 1024);
+          // P of keys 16kk .. 16kk+15: columns 8kk .. 8kk+7, low part 32 further.
+          const uint32_t pa = base + Cfg::kPCol + 8 * kk;
+          tc_mma_ts(base + Cfg::kOCol, pa, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (Cfg::kSplitP) tc_mma_ts(base + Cfg::kOCol, pa + 32, bdesc, Cfg::kIdescPV, 1u);
         }
+        tc_commit(p_free(tt));
       }
       __syncwarp();
     };
+    const int tq = warp - Cfg::kMmaWarp;  // this issuer's Q tile
     bool ok = wait_all(k_full(0), 0);
     if (ok) {
       tc_fence_after();
-      issue_s(0, 0);
-      issue_s(1, 0);
+      issue_s(tq, 0);
     }
-    for (int j = 1; j <= n_tiles && ok; ++j) {
-      const int jp = j - 1, stp = jp % NS;
-      ok = wait_all(p_full(0), jp) && wait_all(v_full(stp), jp / NS);
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      const int st = j % NS;
+      if (j + 1 < n_tiles) {
+        ok = wait_all(k_full((j + 1) % NS), (j + 1) / NS) && wait_all(s_free(tq), j);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(tq, j + 1);
+      }
+      ok = wait_all(p_full(tq), j) && wait_all(v_full(st), j / NS);
       if (!ok) break;
-      if (jp == n_tiles - 1 && n_keys - jp * KT < KT) {
+      if (j == n_tiles - 1 && n_keys - j * KT < KT) {
         // Value rows past the last needed key hold stale pool contents
-        // (0 * NaN would poison O): zero them.
-        const int valid = n_keys - jp * KT;
-        unsigned char* vt = smem + Cfg::kRingOff + stp * Cfg::kStageBytes + Cfg::kTileBytes;
+        // (0 * NaN would poison O): zero them.  Both issuers do it, writing
+        // the same zeros, each before its own last P.V.
+        const int valid = n_keys - j * KT;
+        unsigned char* vt = smem + Cfg::kRingOff + st * Cfg::kStageBytes + Cfg::kKvBytes;
         for (int e = lane; e < (KT - valid) * Cfg::kHalves * 8; e += 32) {
           const int row = valid + e / (Cfg::kHalves * 8);
           const int rest = e % (Cfg::kHalves * 8);
-          *reinterpret_cast<uint4*>(vt + (rest >> 3) * Cfg::kHalfBytes + row * 128 +
+          *reinterpret_cast<uint4*>(vt + (rest >> 3) * Cfg::kKvHalfBytes + row * 128 +
                                     (rest & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_proxy_async_smem();
         __syncwarp();
       }
       tc_fence_after();
-      issue_pv(0, jp);
-      if (j < n_tiles) {
-        ok = wait_all(k_full(j % NS), j / NS);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(0, j);
-      }
-      ok = wait_all(p_full(1), jp);
-      if (!ok) break;
-      tc_fence_after();
-      issue_pv(1, jp);
-      if (lane == 0) tc_commit(kv_empty(stp));
-      if (j < n_tiles) issue_s(1, j);
+      issue_pv(tq, j);
+      if (lane == 0) tc_commit(kv_empty(st));
     }
-    if (ok && lane == 0) tc_commit(o_last);
+    if (ok && lane == 0) tc_commit(o_last(tq));
     failed = !ok;
-    // Every MMA issued has completed before the tensor memory is released.
-    if (lane == 0) tc_commit(drain);
+    // Every MMA this thread issued has completed before the tensor memory
+    // is released.
+    if (lane == 0) tc_commit(drain(tq));
     __syncwarp();
-    mbar_wait(drain, 0);
+    mbar_wait(drain(tq), 0);
   } else {
     // ---- softmax, row rr of Q tile t ----------------------------------------
     const int pos = first + qi;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t scol = t * 128, ocol = Cfg::kOCol + t * D;
+    const uint32_t scol = t * Cfg::kTileCols, pcol = scol + Cfg::kPCol, ocol = scol + Cfg::kOCol;
     const float qscale = p.qscale;
     float m = -INFINITY, l = 0.f;
     bool ok = true;
@@ -381,11 +394,12 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         break;
       }
       tc_fence_after();
-      // The S row (128 scores) in one tensor-memory round trip.  Keys past
-      // this row's position count as -inf; the mask is applied only on
-      // diagonal tiles.
+      // The S row (64 scores), then S is free for the next tile's MMA.
       uint32_t w[KT];
-      tmem_ld128(lane_base + scol, w);
+      tmem_ld64(lane_base + scol, w);
+      tc_fence_before();
+      mbar_arrive(s_free(t));
+      // Keys past this row's position count as -inf (diagonal tiles only).
       const int lim = pos - j * KT;  // keys c <= lim are visible
       if (__any_sync(kFullMask, lim < KT - 1)) {
 #pragma unroll
@@ -399,13 +413,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           mq[u] = max3(mq[u], __uint_as_float(w[c + 2 * u]), __uint_as_float(w[c + 2 * u + 1]));
-      float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
-      mx *= qscale;  // the scale is positive
+      const float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * qscale;  // the scale is positive
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
       // sees key 0 in tile 0, so m is finite from then on.
-      // O is rescaled after P is stored (the scores are dead by then), still
-      // before the P.V that adds this tile.
       bool rescale = false;
       float alpha = 1.f;
       if (j == 0) {
@@ -434,35 +445,36 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         sum2[(c >> 1) & 3] = __fadd2_rn(sum2[(c >> 1) & 3], e);
       }
       const float2 s01 = __fadd2_rn(sum2[0], sum2[1]), s23 = __fadd2_rn(sum2[2], sum2[3]);
-      const float2 st = __fadd2_rn(s01, s23);
-      l += st.x + st.y;
-      // P over S: keys 2c, 2c+1 in column c (high part, or the only one);
-      // the bf16 low part of the same keys in column 64 + c.  Stored in two
-      // halves of 64 keys.
-      if (Cfg::kSplitP) {
+      const float2 sx = __fadd2_rn(s01, s23);
+      l += sx.x + sx.y;
+      // P: keys 2c, 2c+1 in column c (high part, or the only one); the bf16
+      // low part of the same keys in column 32 + c.
+      uint32_t pk[KT];
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t pk[64];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const uint32_t a = w[64 * h + 2 * i], b = w[64 * h + 2 * i + 1];
-            pk[i] = __byte_perm(a, b, 0x7632);  // upper halves: truncated bf16
-            // exact remainders p - trunc(p), rounded to bf16
-            const float2 r = __ffma2_rn(
-                make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
-                make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
-            pk[32 + i] = pack_pair<T>(r.x, r.y);
-          }
-          tmem_st2x32_nowait(lane_base + scol + 32 * h, lane_base + scol + 64 + 32 * h, pk);
+      for (int c = 0; c < KT / 2; ++c) {
+        const uint32_t a = w[2 * c], b = w[2 * c + 1];
+        if (Cfg::kSplitP) {
+          pk[c] = __byte_perm(a, b, 0x7632);  // upper halves: truncated bf16
+          // exact remainders p - trunc(p), rounded to bf16
+          const float2 r = __ffma2_rn(
+              make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
+              make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
+          pk[KT / 2 + c] = pack_pair<T>(r.x, r.y);
+        } else {
+          pk[c] = pack_pair<T>(__uint_as_float(a), __uint_as_float(b));
+          pk[KT / 2 + c] = 0u;
         }
-      } else {
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < KT / 2; ++c)
-          pk[c] = pack_pair<T>(__uint_as_float(w[2 * c]), __uint_as_float(w[2 * c + 1]));
-        tmem_st2x32_nowait(lane_base + scol, lane_base + scol + 32, pk);
       }
-      tmem_wait_st();
+      // P.V of tile j-1 has read P and added into O before either changes.
+      if (j > 0) {
+        ok = mbar_wait(p_free(t), (uint32_t)((j - 1) & 1));
+        if (__any_sync(kFullMask, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      tmem_st64(lane_base + pcol, pk);
       if (rescale) {
 #pragma unroll 1
         for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -478,7 +490,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     }
     // ---- epilogue: O / l into the output rows that are real queries ---------
     if (ok) {
-      ok = mbar_wait(o_last, 0);
+      ok = mbar_wait(o_last(t), 0);
       ok = !__any_sync(kFullMask, !ok);
     }
     failed = !ok;
