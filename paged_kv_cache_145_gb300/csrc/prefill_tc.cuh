@@ -11,31 +11,31 @@
 // Work decomposition (this library's design): one CTA per (query tile, KV
 // head, sequence).  A CTA holds two Q tiles, A and B, of 128 rows each; a
 // row is a (query, grouped head) pair, so the G query heads sharing a KV
-// head share every K/V tile.  Keys stream in tiles of 128 positions.  Ten
+// head share every K/V tile.  Keys stream in tiles of 64 positions.  Eleven
 // warps with fixed roles:
-//   warps 0-7  softmax: warp w serves Q tile w / 4; thread = one row =
-//              one tensor-memory lane: loads its S row from tensor memory,
-//              masks keys past its position, keeps the running maximum and
-//              sum, writes P (16-bit; bf16 as high and low parts) back over
-//              its S buffer, rescales its O row when needed, and finally
-//              normalises and stores O;
+//   warps 0-7  softmax: warp w serves Q tile w / 4; thread = one row = one
+//              tensor-memory lane: loads its S row, releases S, masks keys
+//              past its position, keeps the running maximum and sum, writes
+//              P (16-bit; bf16 as high and low parts) into its own columns,
+//              rescales its O row when needed, and finally normalises and
+//              stores O;
 //   warp 8     producer: 4-D TMA tile loads of K and V pages into a ring
 //              (128-byte swizzle); allocates the tensor memory;
-//   warps 9,10 MMA issuers (one thread each, Q tile A and B): S_t = Q_t.K^T (A and B from shared
-//              memory, 128 x 128 x D) and O_t += P_t.V (A = P_t from tensor
-//              memory, B = V from shared memory in MN-major form,
-//              128 x D x 128), in the order P.V_A(j-1), S_A(j), P.V_B(j-1),
-//              S_B(j): while one tile's softmax runs, the tensor core works
-//              on the other's; zeroes value rows past the last needed key
-//              before the last P.V.
+//   warps 9,10 MMA issuers, one thread each for Q tile A and B:
+//              S_t = Q_t.K^T (A and B from shared memory, 128 x 64 x D) and
+//              O_t += P_t.V (A = P_t from tensor memory, B = V from shared
+//              memory in MN-major form, 128 x D x 64).  S_t(j+1) is issued as
+//              soon as the softmax has read S_t(j), P.V_t(j) once P_t(j) is
+//              written; each issuer zeroes the value rows past the last
+//              needed key before its last P.V.
 // The running maximum is raised lazily: O and the sum are rescaled only
 // when a row's maximum grows by more than 2^8, so P stays at or below 256
 // and most tiles skip the tensor-memory round trip of O.
 //
-// Tensor memory (512 columns): S_A at column 0, S_B at 128, O_A at 256,
-// O_B at 256 + D.  Every wait is bounded; on a timeout the roles stop, the
-// MMA issuer waits for its MMAs to drain, and the tensor memory is released
-// on every path.
+// Tensor memory (512 columns), per Q tile t at t * 256: S at +0 (64
+// columns), P at +64 (64), O at +128 (D).  Every wait is bounded; on a
+// timeout the roles stop, each MMA issuer waits for its MMAs to drain, and
+// the tensor memory is released on every path.
 #pragma once
 
 #include <type_traits>
