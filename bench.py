@@ -54,8 +54,8 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 # KV dtype, with the hash of the sources of that kernel family they were
 # taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b": (1280275968, "118000bf3980d6e6"),
-    "gqa": (1128982784, "118000bf3980d6e6"),
+    "opt13b": (1280424472, "118000bf3980d6e6"),
+    "gqa": (1129142640, "118000bf3980d6e6"),
     "opt13b/fp8": (641224448, "592eb2fee4a7063b"),
     "gqa/fp8": (563400448, "592eb2fee4a7063b"),
 }
