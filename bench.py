@@ -267,55 +267,107 @@ def barrier():
 # ---------------------------------------------------------------------------
 # CPU oracle leg (spawned child, single BLAS thread)
 # ---------------------------------------------------------------------------
-def _oracle_sample(name, budget_s, max_seqs, seed):
-    """Times the oracle's KV write + attention over sequences of the workload
-    until ``budget_s`` seconds have passed; returns (kv_bytes, seconds, seqs)."""
-    from oracle import attention as A
+def _oracle_prepare(name, i, t, seed):
+    """Inputs of one oracle decode step for a sequence of t cached tokens:
+    its pool after the append (slot and table planned by the oracle's block
+    pool), the new key/value and the query.  Not timed."""
     from oracle import blocks as B
     from oracle import paging as P
 
     cfg = synth.CONFIGS[name]
     b, H, Hk, D, dt = cfg["block_size"], cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
-    elt = synth.ELEM_BYTES[dt]
-    lengths = (synth.lengths(name) if name != "fork" else np.full(cfg["groups"] * cfg["forks"], cfg["prompt"]))
+    nblk = P.blocks_needed(t + 1, b)
+    pool = B.BlockPool(nblk, b, free_order=synth.free_order(seed + i, nblk), auto_verify=False)
+    pool.admit(0, list(range(t)))
+    slot = pool.append(0, -1).slot
+    return dict(
+        kp=synth.storage_numpy(synth.normal(seed + 3 * i, (nblk, Hk, b, D), dt), dt),
+        vp=synth.storage_numpy(synth.normal(seed + 3 * i + 1, (nblk, Hk, b, D), dt), dt),
+        kn=synth.storage_numpy(synth.normal(seed + 3 * i + 2, (1, Hk, D), dt), dt),
+        q=synth.storage_numpy(synth.normal(seed + 7 * i, (1, H, D), dt), dt),
+        slot=slot, table=pool.table(0), length=t + 1, b=b, D=D, dt=dt,
+        kv_bytes=2 * (t + 1) * Hk * D * synth.ELEM_BYTES[dt])
+
+
+def _oracle_step(x):
+    """The oracle's KV write + attention for one prepared sequence; seconds."""
+    from oracle import attention as A
+
+    t0 = time.perf_counter()
+    kp2, vp2, _ = A.write_tokens(x["kp"], x["vp"], x["kn"], x["kn"], [x["slot"]], x["b"])
+    A.attention(x["q"], kp2, vp2, [x["table"]], [x["length"]], 1.0 / math.sqrt(x["D"]), x["b"],
+                x["dt"])
+    return time.perf_counter() - t0
+
+
+def _lengths(name):
+    cfg = synth.CONFIGS[name]
+    if name == "fork":
+        return np.full(cfg["groups"] * cfg["forks"], cfg["prompt"])
+    return synth.lengths(name)
+
+
+def _oracle_sample(name, budget_s, seed):
+    """Times the oracle's KV write + attention over sequences of the workload
+    until ``budget_s`` seconds of oracle work have passed; returns
+    (kv_bytes, seconds, seqs)."""
     kv_bytes, done, spent = 0, 0, 0.0
-    for i, t in enumerate(lengths[:max_seqs]):
-        t = int(t)
-        nblk = P.blocks_needed(t + 1, b)
-        pool = B.BlockPool(nblk, b, free_order=synth.free_order(seed + i, nblk), auto_verify=False)
-        pool.admit(0, list(range(t)))
-        kp = synth.storage_numpy(synth.normal(seed + 3 * i, (nblk, Hk, b, D), dt), dt)
-        vp = synth.storage_numpy(synth.normal(seed + 3 * i + 1, (nblk, Hk, b, D), dt), dt)
-        kn = synth.storage_numpy(synth.normal(seed + 3 * i + 2, (1, Hk, D), dt), dt)
-        q = synth.storage_numpy(synth.normal(seed + 7 * i, (1, H, D), dt), dt)
-        t0 = time.perf_counter()
-        slot = pool.append(0, -1).slot
-        kp2, vp2, _ = A.write_tokens(kp, vp, kn, kn, [slot], b)
-        A.attention(q, kp2, vp2, [pool.table(0)], [t + 1], 1.0 / math.sqrt(D), b, dt)
-        spent += time.perf_counter() - t0
-        kv_bytes += 2 * (t + 1) * Hk * D * elt
+    for i, t in enumerate(_lengths(name)):
+        x = _oracle_prepare(name, i, int(t), seed)
+        spent += _oracle_step(x)
+        kv_bytes += x["kv_bytes"]
         done += 1
         if spent >= budget_s:
             break
     return kv_bytes, spent, done
 
 
-def _oracle_child(conn, name, budget_s, max_seqs, seed):
-    conn.send(_oracle_sample(name, budget_s, max_seqs, seed))
+def _reference_steps(name, steps, warmup, seed, distinct=8, target_s=120.0):
+    """The reference arm: warm-up and timed steps of the oracle, each one
+    sequence of the workload (cycling over ``distinct`` prepared ones).
+    So that K + W steps take about ``target_s`` seconds of oracle work,
+    a step covers the first h KV heads of its sequence (with their query
+    heads), h chosen from one timed full step.  Returns (kv_bytes, seconds,
+    steps, h, kv_heads)."""
+    cfg = synth.CONFIGS[name]
+    Hk, G = cfg["kv_heads"], cfg["heads"] // cfg["kv_heads"]
+    lengths = _lengths(name)
+    xs = [_oracle_prepare(name, i, int(lengths[i % len(lengths)]), seed) for i in range(distinct)]
+    full = sum(_oracle_step(x) for x in xs) / distinct
+    h = int(max(1, min(Hk, Hk * target_s / max(steps + warmup, 1) / max(full, 1e-9))))
+    for x in xs:
+        x["kp"], x["vp"] = x["kp"][:, :h].copy(), x["vp"][:, :h].copy()
+        x["kn"], x["q"] = x["kn"][:, :h].copy(), x["q"][:, :h * G].copy()
+        x["kv_bytes"] = x["kv_bytes"] * h // Hk
+    for k in range(warmup):
+        _oracle_step(xs[k % distinct])
+    kv_bytes, spent = 0, 0.0
+    for k in range(steps):
+        spent += _oracle_step(xs[k % distinct])
+        kv_bytes += xs[k % distinct]["kv_bytes"]
+    return kv_bytes, spent, steps, h, Hk
+
+
+def _oracle_child(conn, fn, args):
+    conn.send(fn(*args))
     conn.close()
 
 
-def oracle_timed(name, budget_s, max_seqs=10 ** 9, seed=4242):
-    """Runs the oracle sample in a spawned child limited to one BLAS thread."""
+def oracle_child(fn, *args):
+    """Runs fn(*args) in a spawned child limited to one BLAS thread."""
     for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     ctx = mp.get_context("spawn")
     parent, child = ctx.Pipe()
-    p = ctx.Process(target=_oracle_child, args=(child, name, budget_s, max_seqs, seed))
+    p = ctx.Process(target=_oracle_child, args=(child, fn, args))
     p.start()
     result = parent.recv()
     p.join()
     return result
+
+
+def oracle_timed(name, budget_s, seed=4242):
+    return oracle_child(_oracle_sample, name, budget_s, seed)
 
 
 # ---------------------------------------------------------------------------
@@ -325,12 +377,8 @@ def run_reference(args):
     rank, _, world = dist_env()
     if rank != 0:
         return
-    for _ in range(args.warmup):
-        oracle_timed(args.config, 0.0, max_seqs=1)
-    total_b, total_s, seqs = 0, 0.0, 0
-    for k in range(args.steps):
-        b, s, n = oracle_timed(args.config, 0.0, max_seqs=1, seed=4242 + 1000 * k)
-        total_b, total_s, seqs = total_b + b, total_s + s, seqs + n
+    total_b, total_s, seqs, h, hk = oracle_child(_reference_steps, args.config, args.steps,
+                                                 args.warmup, 4242)
     gbs = total_b / total_s / 1e9
     cfg = synth.CONFIGS[args.config]
     line = {
@@ -339,11 +387,14 @@ def run_reference(args):
         "ms_per_step": round(1e3 * total_s / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.config, "about": cfg["about"],
-                   "sample": "one sequence of the workload per step, all heads"},
-        "decode_tokens_per_s": round(seqs / total_s, 3),
+                   "sample": "one sequence of the workload per step (8 distinct sequences "
+                             "cycled), its first %d of %d KV heads" % (h, hk)},
+        # a step over h of the KV heads counts as h / kv_heads of a sequence
+        "decode_tokens_per_s": round(seqs * h / hk / total_s, 3),
         "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": "%d sequences, one per step, float64 NumPy oracle "
-                                   "(write + attention), 1 BLAS thread" % seqs},
+                         "sample": "%d steps of one sequence each (8 distinct, cycled; "
+                                   "%d of %d KV heads), float64 NumPy oracle (write + "
+                                   "attention), 1 BLAS thread" % (seqs, h, hk)},
         "e2e": {"value": round(gbs, 6), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }

@@ -46,6 +46,18 @@ def test_unique_bytes_count_shared_pages_once():
     assert w.unique_kv_bytes() == w.decode_bytes(512)[1]
 
 
+def test_reference_arm_steps_are_bounded_and_counted():
+    # K + W steps of the oracle in one process; the head count per step is
+    # chosen so the whole run stays near its time target.
+    b, secs, steps, h, hk = bench._reference_steps("tiny", 6, 2, 4242, distinct=2, target_s=60.0)
+    assert steps == 6 and 1 <= h <= hk == 4 and secs > 0
+    lens = bench._lengths("tiny")
+    per = [2 * (int(lens[i]) + 1) * h * 64 * 4 for i in range(2)]
+    assert b == 3 * per[0] + 3 * per[1]
+    _, _, _, h_small, _ = bench._reference_steps("tiny", 20, 0, 4242, distinct=1, target_s=1e-6)
+    assert h_small == 1
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
