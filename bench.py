@@ -56,8 +56,8 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 TRAFFIC = {
     "opt13b": (1280424472, "118000bf3980d6e6"),
     "gqa": (1129142640, "118000bf3980d6e6"),
-    "opt13b/fp8": (641224448, "592eb2fee4a7063b"),
-    "gqa/fp8": (563400448, "592eb2fee4a7063b"),
+    "opt13b/fp8": (644210176, "1ba078747bf5507f"),
+    "gqa/fp8": (565904896, "1ba078747bf5507f"),
 }
 
 KERNEL_SOURCES = {
