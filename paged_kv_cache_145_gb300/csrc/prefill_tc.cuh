@@ -45,10 +45,18 @@
 
 namespace pkv {
 
-template <typename T, int D, int BS, int G>
+// Q tiles per CTA: 2 (one CTA per SM, K/V tiles shared by 256 rows) or 1
+// (two CTAs per SM, each one's set-up and tail overlapping the other's
+// work).  Measured on the 2048-token prompt and chunked workloads: 649 / 759
+// TFLOP/s with 2, 520 / 530 with 1 -- sharing each K/V tile between 256 rows
+// outweighs the overlap.
+constexpr int kPrefillQTiles = 2;
+
+template <typename T, int D, int BS, int G, int QT = kPrefillQTiles>
 struct PrefillTcCfg {
+  static constexpr int kQTiles = QT;
   static constexpr int kTileRows = 128;          // rows per Q tile = tensor-memory lanes
-  static constexpr int kRows = 2 * kTileRows;    // two Q tiles per CTA (A and B)
+  static constexpr int kRows = QT * kTileRows;
   static constexpr int kQueries = kRows / G;     // queries per CTA
   static constexpr int kKeys = 64;               // keys per K/V tile
   static constexpr int kHalves = D / 64;         // 128-byte column blocks
@@ -56,24 +64,25 @@ struct PrefillTcCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;     // one Q tile (128 rows)
   static constexpr int kKvHalfBytes = kKeys * 128;               // 64 key rows x 128 B
   static constexpr int kKvBytes = kHalves * kKvHalfBytes;        // one K or V tile
-  static constexpr int kStages = D == 64 ? 6 : 4;
+  static constexpr int kStages = QT == 2 ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 2);
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
-  static constexpr int kSoftmaxWarps = 8;
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;             // warps 9 and 10: MMA issuers of Q tiles A, B
-  static constexpr int kThreads = 11 * 32;
+  static constexpr int kSoftmaxWarps = 4 * QT;
+  static constexpr int kProducerWarp = 4 * QT;
+  static constexpr int kMmaWarp = 4 * QT + 1;    // one MMA issuer warp per Q tile
+  static constexpr int kThreads = (5 * QT + 1) * 32;
+  static constexpr int kCtasPerSm = QT == 2 ? 1 : 2;
   static constexpr int kQOff = 0;                // Q tile t at t * kTileBytes
-  static constexpr int kRingOff = 2 * kTileBytes;
+  static constexpr int kRingOff = QT * kTileBytes;
   static constexpr int kStageBytes = 2 * kKvBytes;  // K then V
   static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 3 * kStages + 12;
+  static constexpr int kNumBars = 3 * kStages + 6 * QT;
   static constexpr int kSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAlign = 1024;
   static constexpr int kSmemBytes = kAlign + kSlotOff + 16;
   // Tensor memory per Q tile t (base t * 256): S at +0 (64 columns), P at
   // +64 (keys 2c, 2c+1 in column c; bf16 low part in 32 + c), O at +128.
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kTmemCols = 256 * QT;
   static constexpr uint32_t kTileCols = 256;
   static constexpr uint32_t kPCol = 64, kOCol = 128;
   static constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
@@ -84,7 +93,9 @@ struct PrefillTcCfg {
   static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
   static_assert(kBoxes <= 32, "one producer lane per box");
   static_assert(kKeys == 64, "the softmax's P layout assumes 64-key tiles");
-  static_assert(kSmemBytes > 116 * 1024, "one CTA per SM: the tensor memory is not shared");
+  // At most kCtasPerSm CTAs per SM, so that the tensor memory (512 columns
+  // per SM) always covers every resident CTA's allocation.
+  static_assert(kSmemBytes * (kCtasPerSm + 1) > 228 * 1024, "CTAs per SM vs tensor memory");
   static_assert(kOCol + D <= kTileCols, "tensor memory per Q tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
 };
@@ -127,10 +138,12 @@ __device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float lo, float hi)
 }
 
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G>::kThreads, 1)
+__global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G>::kThreads,
+                                  PrefillTcCfg<T, D, BS, G>::kCtasPerSm)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
   using Cfg = PrefillTcCfg<T, D, BS, G>;
+  constexpr int QT = Cfg::kQTiles;
   constexpr int NS = Cfg::kStages;
   constexpr int KT = Cfg::kKeys;
   constexpr int RB = Cfg::kBoxRows;
@@ -193,18 +206,18 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   auto kv_empty = [&](int st) { return bar0 + 8u * (2 * NS + st); };
   // Per Q tile t: S ready, S read (free), P written, P.V done (P free).
   auto s_full = [&](int t) { return bar0 + 8u * (3 * NS + t); };
-  auto s_free = [&](int t) { return bar0 + 8u * (3 * NS + 2 + t); };
-  auto p_full = [&](int t) { return bar0 + 8u * (3 * NS + 4 + t); };
-  auto p_free = [&](int t) { return bar0 + 8u * (3 * NS + 6 + t); };
-  auto drain = [&](int t) { return bar0 + 8u * (3 * NS + 8 + t); };
-  auto o_last = [&](int t) { return bar0 + 8u * (3 * NS + 10 + t); };  // last P.V (single use)
+  auto s_free = [&](int t) { return bar0 + 8u * (3 * NS + QT + t); };
+  auto p_full = [&](int t) { return bar0 + 8u * (3 * NS + 2 * QT + t); };
+  auto p_free = [&](int t) { return bar0 + 8u * (3 * NS + 3 * QT + t); };
+  auto drain = [&](int t) { return bar0 + 8u * (3 * NS + 4 * QT + t); };
+  auto o_last = [&](int t) { return bar0 + 8u * (3 * NS + 5 * QT + t); };  // last P.V (single use)
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
       mbar_init(k_full(st), 1);
       mbar_init(v_full(st), 1);
-      mbar_init(kv_empty(st), 2);  // both Q tiles' P.V
+      mbar_init(kv_empty(st), QT);  // every Q tile's P.V
     }
-    for (int t = 0; t < 2; ++t) {
+    for (int t = 0; t < QT; ++t) {
       mbar_init(s_full(t), 1);
       mbar_init(s_free(t), Cfg::kTileRows);
       mbar_init(p_full(t), Cfg::kTileRows);
@@ -224,7 +237,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   // min(qa + R / G, Q - 1) (padding rows repeat the last query and are not
   // stored), head kvh * G + R % G.  It copies its Q row into the
   // 128-byte-swizzled operand layout.
-  const int t = (warp >> 2) & 1;
+  const int t = (warp >> 2) & (QT - 1);
   const int rr = (warp & 3) * 32 + lane;
   const int R = t * Cfg::kTileRows + rr;
   const int qi = min(qa + R / G, Q - 1);
