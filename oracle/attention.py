@@ -281,7 +281,7 @@ def attention(q, k_pool, v_pool, tables, seq_lens, scale, b, dtype, seqs=None, m
 
 
 def prefill_attention(q, k_pool, v_pool, tables, seq_lens, query_starts, scale, b, dtype,
-                      seqs=None):
+                      seqs=None, q_dtype=None, k_scale=None, v_scale=None):
     """Causal attention of a chunk of new queries per sequence (prefill).
 
     "vLLM and PagedAttention: Virtual Memory for LLM Serving" (opening
@@ -298,6 +298,9 @@ def prefill_attention(q, k_pool, v_pool, tables, seq_lens, query_starts, scale, 
 
     ``q``: ``[total queries, H, D]``; pools ``[N, Hk, b, D]``; returns
     ``out float64 [total queries, H, D]`` (rows of unlisted sequences NaN).
+    For an FP8 (``"e4m3"``) pool, ``q`` is stored in ``q_dtype`` and the
+    key/value rows of KV head kh are the codes' values times ``k_scale[kh]``
+    / ``v_scale[kh]``, as in :func:`attention`.
     """
     q = np.asarray(q)
     _, n_heads, dim = q.shape
@@ -313,10 +316,14 @@ def prefill_attention(q, k_pool, v_pool, tables, seq_lens, query_starts, scale, 
         for kvh in range(kv_heads):
             keys = to_f64(gather_rows(k_pool, table, length, b, kvh), dtype)
             vals = to_f64(gather_rows(v_pool, table, length, b, kvh), dtype)
+            if k_scale is not None:
+                keys = keys * float(k_scale[kvh])
+            if v_scale is not None:
+                vals = vals * float(v_scale[kvh])
             for h in range(kvh * group, (kvh + 1) * group):
                 for i in range(q1 - q0):
                     visible = first + i + 1
-                    z = scale * (keys[:visible] @ to_f64(q[q0 + i, h], dtype))
+                    z = scale * (keys[:visible] @ to_f64(q[q0 + i, h], q_dtype or dtype))
                     w = np.exp(z - z.max())
                     out[q0 + i, h] = (w @ vals[:visible]) / w.sum()
     return out

@@ -529,3 +529,27 @@ def check_fp8_write_and_attention(write_tokens_fp8, dequantize_pool, attention, 
     ref, _ = attention(q.astype(np.float64), dequantize_pool(k2, ks), dequantize_pool(v2, vs), tables,
                        lens, 0.3, b, "f64")
     assert np.max(np.abs(out - ref)) < 1e-12
+
+
+def check_fp8_prefill(prefill_attention, attention, dequantize_pool):
+    """Causal prefill over an FP8 pool equals prefill over its dequantized
+    float64 values, and one-query chunks equal FP8 decode attention."""
+    rng = np.random.default_rng(17)
+    n, hk, b, d, g = 8, 2, 4, 8, 2
+    kp = rng.integers(0, 0x7E, size=(n, hk, b, d)).astype(np.uint8)
+    vp = rng.integers(0, 0x7E, size=(n, hk, b, d)).astype(np.uint8)
+    kp[kp % 3 == 0] |= 0x80  # some negative codes
+    ks, vs = np.array([0.03, 0.2], np.float32), np.array([0.05, 0.01], np.float32)
+    tables, lens = [[6, 1, 3], [0, 4, 2, 5]], [11, 14]
+    starts = np.array([0, 4, 9])  # chunks of 4 and 5 new queries
+    q = rng.standard_normal((9, hk * g, d)).astype(np.float16)
+    out = prefill_attention(q, kp, vp, tables, lens, starts, 0.25, b, "e4m3", q_dtype="f16",
+                            k_scale=ks, v_scale=vs)
+    ref = prefill_attention(q.astype(np.float64), dequantize_pool(kp, ks), dequantize_pool(vp, vs),
+                            tables, lens, starts, 0.25, b, "f64")
+    assert np.max(np.abs(out - ref)) < 1e-12
+    # The last query of each chunk sees the whole sequence: decode attention.
+    last = [int(starts[1]) - 1, int(starts[2]) - 1]
+    dec, _ = attention(q[last], kp, vp, tables, lens, 0.25, b, "e4m3", q_dtype="f16", k_scale=ks,
+                       v_scale=vs)
+    assert np.max(np.abs(out[last] - dec)) < 1e-12

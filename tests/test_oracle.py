@@ -99,3 +99,7 @@ def test_e4m3():
 def test_fp8_write_and_attention():
     pins.check_fp8_write_and_attention(A.write_tokens_fp8, A.dequantize_pool, A.attention,
                                        A.e4m3_encode)
+
+
+def test_fp8_prefill():
+    pins.check_fp8_prefill(A.prefill_attention, A.attention, A.dequantize_pool)

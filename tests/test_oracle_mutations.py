@@ -131,3 +131,14 @@ def test_e4m3_ties_away_from_even():
 def test_e4m3_wrong_bias():
     bad = mutant(A.e4m3_decode, "2.0 ** (exp - 7.0)", "2.0 ** (exp - 8.0)")
     fails(pins.check_e4m3, A.e4m3_encode, bad)
+
+
+def test_fp8_prefill_value_scale_on_keys():
+    bad = mutant(A.prefill_attention, "keys = keys * float(k_scale[kvh])",
+                 "keys = keys * float(v_scale[kvh])")
+    fails(pins.check_fp8_prefill, bad, A.attention, A.dequantize_pool)
+
+
+def test_fp8_prefill_missing_value_scale():
+    bad = mutant(A.prefill_attention, "vals = vals * float(v_scale[kvh])", "vals = vals")
+    fails(pins.check_fp8_prefill, bad, A.attention, A.dequantize_pool)
