@@ -30,6 +30,8 @@ int pkv_launch_prefill_tc_f16(const pkv::PrefillParams&, int, int, int, int, con
                               const CUtensorMap&, cudaStream_t);
 int pkv_launch_prefill_tc_bf16(const pkv::PrefillParams&, int, int, int, int, const CUtensorMap&,
                                const CUtensorMap&, cudaStream_t);
+int pkv_launch_prefill_tc_fp8(const pkv::PrefillParams&, int, int, int, int, int,
+                              const CUtensorMap&, const CUtensorMap&, cudaStream_t);
 int pkv_launch_decode_f32(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
                           cudaStream_t);
 int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
@@ -353,9 +355,13 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
     return PKV_ERR_ARG;
   if (num_seqs == 0 || total_queries == 0) return PKV_OK;
   if (!q || !out || !query_starts || !block_tables || !seq_lens) return PKV_ERR_NULL;
-  if (cache->dtype == PKV_F32 || cache->dtype == PKV_FP8_E4M3 ||
-      !decode_geometry_ok(cache, num_heads))
+  // FP8 pools: the tcgen05 kernel only, head_dim 128.
+  const bool fp8 = cache->dtype == PKV_FP8_E4M3;
+  if (cache->dtype == PKV_F32 || !decode_geometry_ok(cache, num_heads) ||
+      (fp8 && (cache->head_dim != 128 || prefill_mma_forced())))
     return PKV_ERR_GEOMETRY;
+  rc = check_scales(cache);
+  if (rc) return rc;
   if (cache->num_kv_heads > 65535 || (int64_t)max_blocks_per_seq * cache->block_size > INT32_MAX)
     return PKV_ERR_ARG;
   if (!aligned16(q) || !aligned16(out) || (reinterpret_cast<uintptr_t>(block_tables) & 3u) ||
@@ -384,12 +390,17 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
   p.max_queries = max_queries;
   p.qscale = scale * 1.4426950408889634f;
   p.err = err;
+  p.k_scale = cache->k_scale;
+  p.v_scale = cache->v_scale;
   const int group = num_heads / cache->num_kv_heads;
   const bool f16 = cache->dtype == PKV_F16;
   if (prefill_mma_forced())
     return (f16 ? pkv_launch_prefill_f16 : pkv_launch_prefill_bf16)(
         p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv, stream);
   if (cache->num_blocks > INT32_MAX) return PKV_ERR_ARG;  // block coordinates are 32-bit
+  if (fp8)
+    return pkv_launch_prefill_tc_fp8(p, cache->io_dtype, num_seqs, cache->head_dim,
+                                     cache->block_size, group, mk, mv, stream);
   return (f16 ? pkv_launch_prefill_tc_f16 : pkv_launch_prefill_tc_bf16)(
       p, num_seqs, cache->head_dim, cache->block_size, group, mk, mv, stream);
 }

@@ -43,6 +43,8 @@ struct PrefillParams {
   int max_queries;         // host bound on queries per sequence
   float qscale;            // scale * log2(e)
   unsigned* err;
+  const float* k_scale;    // FP8 pools: [Hk] key / value scales (else unused)
+  const float* v_scale;
 };
 
 template <typename T, int D, int BS, int G>

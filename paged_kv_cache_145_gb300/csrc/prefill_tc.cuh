@@ -40,6 +40,7 @@
 
 #include <type_traits>
 
+#include "decode_mma_fp8.cuh"
 #include "prefill.cuh"
 #include "tcgen05.cuh"
 
@@ -52,9 +53,13 @@ namespace pkv {
 // outweighs the overlap.
 constexpr int kPrefillQTiles = 2;
 
-template <typename T, int D, int BS, int G, int QT = kPrefillQTiles>
+// KV8: the pool holds FP8 E4M3 codes (keys and values times per-KV-head
+// scales); T is then the type of q and out.  Converter warps widen each K/V
+// tile to fp16 (exact for every E4M3 value), so both products run in fp16.
+template <typename T, int D, int BS, int G, int QT = kPrefillQTiles, bool KV8 = false>
 struct PrefillTcCfg {
   static constexpr int kQTiles = QT;
+  static constexpr bool kKv8 = KV8;
   static constexpr int kTileRows = 128;          // rows per Q tile = tensor-memory lanes
   static constexpr int kRows = QT * kTileRows;
   static constexpr int kQueries = kRows / G;     // queries per CTA
@@ -64,19 +69,27 @@ struct PrefillTcCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;     // one Q tile (128 rows)
   static constexpr int kKvHalfBytes = kKeys * 128;               // 64 key rows x 128 B
   static constexpr int kKvBytes = kHalves * kKvHalfBytes;        // one K or V tile
-  static constexpr int kStages = QT == 2 ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 2);
+  static constexpr int kStages =
+      KV8 ? 2 : (QT == 2 ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 2));  // widened K/V ring
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
   static constexpr int kSoftmaxWarps = 4 * QT;
   static constexpr int kProducerWarp = 4 * QT;
   static constexpr int kMmaWarp = 4 * QT + 1;    // one MMA issuer warp per Q tile
-  static constexpr int kThreads = (5 * QT + 1) * 32;
+  static constexpr int kConvWarp = 5 * QT + 1;  // FP8 pools: converter warps
+  static constexpr int kConvWarps = KV8 ? 4 : 0;
+  static constexpr int kConvThreads = kConvWarps * 32;
+  static constexpr int kThreads = (5 * QT + 1 + kConvWarps) * 32;
   static constexpr int kCtasPerSm = QT == 2 ? 1 : 2;
   static constexpr int kQOff = 0;                // Q tile t at t * kTileBytes
   static constexpr int kRingOff = QT * kTileBytes;
   static constexpr int kStageBytes = 2 * kKvBytes;  // K then V
-  static constexpr int kBarOff = kRingOff + kStages * kStageBytes;
-  static constexpr int kNumBars = 3 * kStages + 6 * QT;
+  // FP8 pools: raw code tiles (64 rows x D codes, 128-byte swizzle), K then V.
+  static constexpr int kRawStages = KV8 ? 4 : 0;
+  static constexpr int kRawBytes = kKeys * D;
+  static constexpr int kRawOff = kRingOff + kStages * kStageBytes;
+  static constexpr int kBarOff = kRawOff + kRawStages * 2 * kRawBytes;
+  static constexpr int kNumBars = 3 * kStages + 6 * QT + 2 * kRawStages;
   static constexpr int kSlotOff = kBarOff + kNumBars * 8;
   static constexpr int kAlign = 1024;
   static constexpr int kSmemBytes = kAlign + kSlotOff + 16;
@@ -85,12 +98,14 @@ struct PrefillTcCfg {
   static constexpr uint32_t kTmemCols = 256 * QT;
   static constexpr uint32_t kTileCols = 256;
   static constexpr uint32_t kPCol = 64, kOCol = 128;
-  static constexpr uint32_t kFmt = std::is_same<T, __nv_bfloat16>::value ? 1u : 0u;
+  // MMA operand type: the pool's type, or fp16 for FP8 pools.
+  using OpT = typename std::conditional<KV8, __half, T>::type;
+  static constexpr uint32_t kFmt = std::is_same<OpT, __nv_bfloat16>::value ? 1u : 0u;
   static constexpr uint32_t kIdescS = idesc_f16(kFmt, 128, kKeys, false);
   static constexpr uint32_t kIdescPV = idesc_f16(kFmt, 128, D, true);
   // bf16 P keeps 8 significant bits; split into high and low bf16 parts
   // (two P.V MMAs) it keeps ~16, like the fp32 softmax it comes from.
-  static constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
+  static constexpr bool kSplitP = !KV8 && std::is_same<T, __nv_bfloat16>::value;
   static_assert(kBoxes <= 32, "one producer lane per box");
   static_assert(kKeys == 64, "the softmax's P layout assumes 64-key tiles");
   // At most kCtasPerSm CTAs per SM, so that the tensor memory (512 columns
@@ -98,6 +113,7 @@ struct PrefillTcCfg {
   static_assert(kSmemBytes * (kCtasPerSm + 1) > 228 * 1024, "CTAs per SM vs tensor memory");
   static_assert(kOCol + D <= kTileCols, "tensor memory per Q tile");
   static_assert(kSmemBytes <= 227 * 1024, "shared memory");
+  static_assert(!KV8 || D == 128, "FP8 pools: 128-code rows");
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -137,12 +153,13 @@ __device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float lo, float hi)
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G>::kThreads,
-                                  PrefillTcCfg<T, D, BS, G>::kCtasPerSm)
+template <typename T, int D, int BS, int G, bool KV8>
+__global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>::kThreads,
+                                  PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>::kCtasPerSm)
 prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv) {
-  using Cfg = PrefillTcCfg<T, D, BS, G>;
+  using Cfg = PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>;
+  constexpr int NR = Cfg::kRawStages;
   constexpr int QT = Cfg::kQTiles;
   constexpr int NS = Cfg::kStages;
   constexpr int KT = Cfg::kKeys;
@@ -211,10 +228,15 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   auto p_free = [&](int t) { return bar0 + 8u * (3 * NS + 3 * QT + t); };
   auto drain = [&](int t) { return bar0 + 8u * (3 * NS + 4 * QT + t); };
   auto o_last = [&](int t) { return bar0 + 8u * (3 * NS + 5 * QT + t); };  // last P.V (single use)
+  // FP8 pools: raw code tiles landed / converted.
+  auto raw_full = [&](int rs) { return bar0 + 8u * (3 * NS + 6 * QT + rs); };
+  auto raw_empty = [&](int rs) { return bar0 + 8u * (3 * NS + 6 * QT + NR + rs); };
   if (threadIdx.x == 0) {
     for (int st = 0; st < NS; ++st) {
-      mbar_init(k_full(st), 1);
-      mbar_init(v_full(st), 1);
+      // Native pools: the producer's copy completes the stage; FP8 pools:
+      // every converter thread arrives once it has widened its part.
+      mbar_init(k_full(st), KV8 ? Cfg::kConvThreads : 1);
+      mbar_init(v_full(st), KV8 ? Cfg::kConvThreads : 1);
       mbar_init(kv_empty(st), QT);  // every Q tile's P.V
     }
     for (int t = 0; t < QT; ++t) {
@@ -224,6 +246,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       mbar_init(p_free(t), 1);
       mbar_init(drain(t), 1);
       mbar_init(o_last(t), 1);
+    }
+    for (int rs = 0; rs < NR; ++rs) {
+      mbar_init(raw_full(rs), 1);
+      mbar_init(raw_empty(rs), Cfg::kConvThreads);
     }
     fence_mbar_init();
   }
@@ -241,15 +267,51 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   const int rr = (warp & 3) * 32 + lane;
   const int R = t * Cfg::kTileRows + rr;
   const int qi = min(qa + R / G, Q - 1);
+  float row_scale = 1.f;  // FP8 pools: this row's factor on its scores
   if (warp < Cfg::kSoftmaxWarps) {
     const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
                                                        ((int64_t)(q0 + qi) * H + kvh * G + R % G) * D);
     unsigned char* qt = smem + Cfg::kQOff + t * Cfg::kTileBytes;
+    uint4 qv[D / 8];
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qv[c] = qrow[c];
+    if constexpr (KV8) {
+      // The MMAs run in fp16.  A bf16 row whose largest magnitude reaches
+      // 2^15 is first scaled by a power of two (exact; undone in the row's
+      // score factor) so that it stays inside fp16's range.
+      row_scale = p.k_scale[kvh];
+      if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+        float amax = 0.f;
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(&qv[c]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)),
+                                     fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+        }
+        float shrink = 1.f;
+        if (amax >= 32768.f && amax <= 3.0e38f) {
+          int e = 0;
+          frexpf(amax, &e);  // amax = m * 2^e, m in [0.5, 1)
+          shrink = ldexpf(1.f, 15 - e);
+          row_scale = ldexpf(row_scale, e - 15);
+        }
+#pragma unroll
+        for (int c = 0; c < D / 8; ++c) {
+          uint32_t* w = reinterpret_cast<uint32_t*>(&qv[c]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            w[i] = pack_pair<__half>(__uint_as_float(w[i] << 16) * shrink,
+                                     __uint_as_float(w[i] & 0xFFFF0000u) * shrink);
+        }
+      }
+    }
 #pragma unroll
     for (int c = 0; c < D / 8; ++c) {
       const int half = c >> 3, cc = c & 7;
       *reinterpret_cast<uint4*>(qt + half * Cfg::kHalfBytes + rr * 128 + ((cc ^ (rr & 7)) << 4)) =
-          qrow[c];
+          qv[c];
     }
     fence_proxy_async_smem();
   }
@@ -261,25 +323,39 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 
   if (warp == Cfg::kProducerWarp) {
     // ---- producer: K and V tiles ------------------------------------------
+    // Native pools: straight into the operand ring.  FP8 pools: raw code
+    // tiles into their own ring, for the converter warps.
     const uint64_t policy = policy_evict_last();
     const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
+    constexpr int RING = KV8 ? NR : NS;
     int issued = 0;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j % NS;
-      if (j >= NS) {
-        const bool ok = mbar_wait(kv_empty(st), (uint32_t)(((j / NS) - 1) & 1));
+      const int st = j % RING;
+      if (j >= RING) {
+        const uint32_t empty = KV8 ? raw_empty(st) : kv_empty(st);
+        const bool ok = mbar_wait(empty, (uint32_t)(((j / RING) - 1) & 1));
         if (__any_sync(kFullMask, !ok)) {
           failed = true;
           break;
         }
       }
-      if (lane == 0) {
-        mbar_arrive_expect_tx(k_full(st), Cfg::kKvBytes);
-        mbar_arrive_expect_tx(v_full(st), Cfg::kKvBytes);
+      uint32_t kdst, vdst, kbar, vbar;
+      if constexpr (KV8) {
+        kdst = sbase + Cfg::kRawOff + st * 2 * Cfg::kRawBytes;
+        vdst = kdst + Cfg::kRawBytes;
+        kbar = vbar = raw_full(st);
+        if (lane == 0) mbar_arrive_expect_tx(kbar, 2 * Cfg::kRawBytes);
+      } else {
+        kdst = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
+        vdst = kdst + Cfg::kKvBytes;
+        kbar = k_full(st);
+        vbar = v_full(st);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(kbar, Cfg::kKvBytes);
+          mbar_arrive_expect_tx(vbar, Cfg::kKvBytes);
+        }
       }
       __syncwarp();
-      const uint32_t kdst = sbase + Cfg::kRingOff + st * Cfg::kStageBytes;
-      const uint32_t vdst = kdst + Cfg::kKvBytes;
       if (lane < Cfg::kBoxes) {
         const int pos = j * KT + lane * RB;
         // Boxes wholly past the last needed key read an out-of-range block:
@@ -289,21 +365,30 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           pb = trow[pos / BS];
           row = pos % BS;
         }
+        if constexpr (KV8) {  // rows of 128 codes: one box per RB rows
+          tma_load_4d(kdst + lane * RB * 128, &tmk, 0, row, kvh, pb, kbar, policy);
+          tma_load_4d(vdst + lane * RB * 128, &tmv, 0, row, kvh, pb, vbar, policy);
+        } else {
 #pragma unroll
-        for (int h = 0; h < Cfg::kHalves; ++h) {
-          const uint32_t o = h * Cfg::kKvHalfBytes + lane * RB * 128;
-          tma_load_4d(kdst + o, &tmk, h * 64, row, kvh, pb, k_full(st), policy);
-          tma_load_4d(vdst + o, &tmv, h * 64, row, kvh, pb, v_full(st), policy);
+          for (int h = 0; h < Cfg::kHalves; ++h) {
+            const uint32_t o = h * Cfg::kKvHalfBytes + lane * RB * 128;
+            tma_load_4d(kdst + o, &tmk, h * 64, row, kvh, pb, kbar, policy);
+            tma_load_4d(vdst + o, &tmv, h * 64, row, kvh, pb, vbar, policy);
+          }
         }
       }
       issued = j + 1;
     }
     // Copies issued but possibly never consumed (another role stopped).
-    for (int j = issued - NS < 0 ? 0 : issued - NS; j < issued; ++j) {
-      mbar_wait(k_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
-      mbar_wait(v_full(j % NS), (uint32_t)((j / NS) & 1), kWaitLimitNs / 8);
+    for (int j = issued - RING < 0 ? 0 : issued - RING; j < issued; ++j) {
+      if constexpr (KV8) {
+        mbar_wait(raw_full(j % RING), (uint32_t)((j / RING) & 1), kWaitLimitNs / 8);
+      } else {
+        mbar_wait(k_full(j % RING), (uint32_t)((j / RING) & 1), kWaitLimitNs / 8);
+        mbar_wait(v_full(j % RING), (uint32_t)((j / RING) & 1), kWaitLimitNs / 8);
+      }
     }
-  } else if (warp >= Cfg::kMmaWarp) {
+  } else if (warp >= Cfg::kMmaWarp && warp < Cfg::kMmaWarp + QT) {
     // ---- MMA issuers, one per Q tile t: S_t(0); then per K/V tile j:
     //      S_t(j+1) once the softmax has read S_t(j), and P.V_t(j) once
     //      P_t(j) is written.  The next S is computed while the softmax works
@@ -366,10 +451,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       }
       ok = wait_all(p_full(tq), j) && wait_all(v_full(st), j / NS);
       if (!ok) break;
-      if (j == n_tiles - 1 && n_keys - j * KT < KT) {
+      if (!KV8 && j == n_tiles - 1 && n_keys - j * KT < KT) {
         // Value rows past the last needed key hold stale pool contents
         // (0 * NaN would poison O): zero them.  Both issuers do it, writing
-        // the same zeros, each before its own last P.V.
+        // the same zeros, each before its own last P.V.  (FP8 pools: the
+        // converters write zeros there.)
         const int valid = n_keys - j * KT;
         unsigned char* vt = smem + Cfg::kRingOff + st * Cfg::kStageBytes + Cfg::kKvBytes;
         for (int e = lane; e < (KT - valid) * Cfg::kHalves * 8; e += 32) {
@@ -392,12 +478,63 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     if (lane == 0) tc_commit(drain(tq));
     __syncwarp();
     mbar_wait(drain(tq), 0);
+  } else if (KV8 && warp >= Cfg::kConvWarp) {
+    // ---- converters (FP8 pools): raw code tiles -> fp16 operand tiles ------
+    // Thread ct widens 16-code chunks of K and then V: chunk ch of key row
+    // r (swizzled in the raw tile) becomes dims 16ch .. 16ch+15, i.e. two
+    // 16-byte chunks of the 128-byte-swizzled fp16 tile.  Value rows at or
+    // past the last needed key are written as zeros (stale codes could be
+    // NaN, and 0 * NaN would poison O).
+    const int ct = threadIdx.x - Cfg::kConvWarp * 32;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int rs = j % NR, st = j % NS;
+      bool ok = mbar_wait(raw_full(rs), (uint32_t)((j / NR) & 1));
+      if (ok && j >= NS) ok = mbar_wait(kv_empty(st), (uint32_t)(((j / NS) - 1) & 1));
+      if (__any_sync(kFullMask, !ok)) {
+        failed = true;
+        break;
+      }
+      const unsigned char* raw = smem + Cfg::kRawOff + rs * 2 * Cfg::kRawBytes;
+      unsigned char* wide = smem + Cfg::kRingOff + st * Cfg::kStageBytes;
+      const int valid = n_keys - j * KT;
+#pragma unroll
+      for (int kv = 0; kv < 2; ++kv) {
+        const unsigned char* src = raw + kv * Cfg::kRawBytes;
+        unsigned char* dst = wide + kv * Cfg::kKvBytes;
+#pragma unroll
+        for (int i = 0; i < KT * 8 / Cfg::kConvThreads; ++i) {
+          const int unit = ct + i * Cfg::kConvThreads;
+          const int row = unit >> 3, ch = unit & 7;
+          uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+          if (kv == 0 || row < valid) {
+            const uint4 c =
+                *reinterpret_cast<const uint4*>(src + row * 128 + ((ch ^ (row & 7)) << 4));
+            e4m3x4_to_f16x4(c.x, lo.x, lo.y);
+            e4m3x4_to_f16x4(c.y, lo.z, lo.w);
+            e4m3x4_to_f16x4(c.z, hi.x, hi.y);
+            e4m3x4_to_f16x4(c.w, hi.z, hi.w);
+          }
+          const int c2 = (ch & 3) * 2;
+          unsigned char* drow = dst + (ch >> 2) * Cfg::kKvHalfBytes + row * 128;
+          *reinterpret_cast<uint4*>(drow + ((c2 ^ (row & 7)) << 4)) = lo;
+          *reinterpret_cast<uint4*>(drow + (((c2 + 1) ^ (row & 7)) << 4)) = hi;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(kv == 0 ? k_full(st) : v_full(st));
+      }
+      mbar_arrive(raw_empty(rs));
+    }
   } else {
     // ---- softmax, row rr of Q tile t ----------------------------------------
     const int pos = first + qi;
     const uint32_t lane_base = tmem + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t scol = t * Cfg::kTileCols, pcol = scol + Cfg::kPCol, ocol = scol + Cfg::kOCol;
-    const float qscale = p.qscale;
+    // Scores are taken as s * |factor| with the sign folded into s, so the
+    // row maximum can be found on the raw scores (a negative factor flips
+    // every score's sign bit first).  FP8 pools: key scale and row shift.
+    const float qfac = p.qscale * row_scale;
+    const bool qneg = qfac < 0.f;
+    const float qscale = fabsf(qfac);
     float m = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
@@ -412,6 +549,10 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       tmem_ld64(lane_base + scol, w);
       tc_fence_before();
       mbar_arrive(s_free(t));
+      if (qneg) {
+#pragma unroll
+        for (int c = 0; c < KT; ++c) w[c] ^= 0x80000000u;
+      }
       // Keys past this row's position count as -inf (diagonal tiles only).
       const int lim = pos - j * KT;  // keys c <= lim are visible
       if (__any_sync(kFullMask, lim < KT - 1)) {
@@ -426,7 +567,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
 #pragma unroll
         for (int u = 0; u < 4; ++u)
           mq[u] = max3(mq[u], __uint_as_float(w[c + 2 * u]), __uint_as_float(w[c + 2 * u + 1]));
-      const float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * qscale;  // the scale is positive
+      const float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * qscale;
       // Lazy maximum: raise it (and rescale O and l) only when the tile's
       // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Every row
       // sees key 0 in tile 0, so m is finite from then on.
@@ -472,9 +613,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           const float2 r = __ffma2_rn(
               make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
               make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
-          pk[KT / 2 + c] = pack_pair<T>(r.x, r.y);
+          pk[KT / 2 + c] = pack_pair<typename Cfg::OpT>(r.x, r.y);
         } else {
-          pk[c] = pack_pair<T>(__uint_as_float(a), __uint_as_float(b));
+          pk[c] = pack_pair<typename Cfg::OpT>(__uint_as_float(a), __uint_as_float(b));
           pk[KT / 2 + c] = 0u;
         }
       }
@@ -510,7 +651,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     if (ok) {
       tc_fence_after();
       const bool real = qa + R / G < qend;
-      const float inv = 1.f / l;
+      const float inv = (KV8 ? p.v_scale[kvh] : 1.f) / l;
       uint4* orow = reinterpret_cast<uint4*>(out + ((int64_t)(q0 + qi) * H + kvh * G + R % G) * D);
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -539,11 +680,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   if (warp == Cfg::kProducerWarp) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
-template <typename T, int D, int BS, int G>
+template <typename T, int D, int BS, int G, bool KV8>
 int launch_prefill_tc_cfg(const PrefillParams& p, int num_seqs, const CUtensorMap& mk,
                           const CUtensorMap& mv, cudaStream_t stream) {
-  using Cfg = PrefillTcCfg<T, D, BS, G>;
-  auto kern = prefill_tc_kernel<T, D, BS, G>;
+  using Cfg = PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>;
+  auto kern = prefill_tc_kernel<T, D, BS, G, KV8>;
   static std::atomic<uint64_t> ready{0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return PKV_ERR_CUDA;
@@ -560,31 +701,47 @@ int launch_prefill_tc_cfg(const PrefillParams& p, int num_seqs, const CUtensorMa
   return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-template <typename T, int D, int BS>
+template <typename T, int D, int BS, bool KV8>
 int launch_prefill_tc_g(const PrefillParams& p, int num_seqs, int group, const CUtensorMap& mk,
                         const CUtensorMap& mv, cudaStream_t stream) {
   switch (group) {
-    case 1: return launch_prefill_tc_cfg<T, D, BS, 1>(p, num_seqs, mk, mv, stream);
-    case 2: return launch_prefill_tc_cfg<T, D, BS, 2>(p, num_seqs, mk, mv, stream);
-    case 4: return launch_prefill_tc_cfg<T, D, BS, 4>(p, num_seqs, mk, mv, stream);
-    case 8: return launch_prefill_tc_cfg<T, D, BS, 8>(p, num_seqs, mk, mv, stream);
+    case 1: return launch_prefill_tc_cfg<T, D, BS, 1, KV8>(p, num_seqs, mk, mv, stream);
+    case 2: return launch_prefill_tc_cfg<T, D, BS, 2, KV8>(p, num_seqs, mk, mv, stream);
+    case 4: return launch_prefill_tc_cfg<T, D, BS, 4, KV8>(p, num_seqs, mk, mv, stream);
+    case 8: return launch_prefill_tc_cfg<T, D, BS, 8, KV8>(p, num_seqs, mk, mv, stream);
   }
   return PKV_ERR_GEOMETRY;
 }
 
+// 16-bit pools: T is the cache and I/O type.
 template <typename T>
 int launch_prefill_tc(const PrefillParams& p, int num_seqs, int head_dim, int block_size,
                       int group, const CUtensorMap& mk, const CUtensorMap& mv,
                       cudaStream_t stream) {
   switch (head_dim * 1000 + block_size) {
-    case 64008: return launch_prefill_tc_g<T, 64, 8>(p, num_seqs, group, mk, mv, stream);
-    case 64016: return launch_prefill_tc_g<T, 64, 16>(p, num_seqs, group, mk, mv, stream);
-    case 64032: return launch_prefill_tc_g<T, 64, 32>(p, num_seqs, group, mk, mv, stream);
-    case 64064: return launch_prefill_tc_g<T, 64, 64>(p, num_seqs, group, mk, mv, stream);
-    case 128008: return launch_prefill_tc_g<T, 128, 8>(p, num_seqs, group, mk, mv, stream);
-    case 128016: return launch_prefill_tc_g<T, 128, 16>(p, num_seqs, group, mk, mv, stream);
-    case 128032: return launch_prefill_tc_g<T, 128, 32>(p, num_seqs, group, mk, mv, stream);
-    case 128064: return launch_prefill_tc_g<T, 128, 64>(p, num_seqs, group, mk, mv, stream);
+    case 64008: return launch_prefill_tc_g<T, 64, 8, false>(p, num_seqs, group, mk, mv, stream);
+    case 64016: return launch_prefill_tc_g<T, 64, 16, false>(p, num_seqs, group, mk, mv, stream);
+    case 64032: return launch_prefill_tc_g<T, 64, 32, false>(p, num_seqs, group, mk, mv, stream);
+    case 64064: return launch_prefill_tc_g<T, 64, 64, false>(p, num_seqs, group, mk, mv, stream);
+    case 128008: return launch_prefill_tc_g<T, 128, 8, false>(p, num_seqs, group, mk, mv, stream);
+    case 128016: return launch_prefill_tc_g<T, 128, 16, false>(p, num_seqs, group, mk, mv, stream);
+    case 128032: return launch_prefill_tc_g<T, 128, 32, false>(p, num_seqs, group, mk, mv, stream);
+    case 128064: return launch_prefill_tc_g<T, 128, 64, false>(p, num_seqs, group, mk, mv, stream);
+  }
+  return PKV_ERR_GEOMETRY;
+}
+
+// FP8 pools (head_dim 128): T is the I/O type of q and out.
+template <typename T>
+int launch_prefill_tc_fp8(const PrefillParams& p, int num_seqs, int head_dim, int block_size,
+                          int group, const CUtensorMap& mk, const CUtensorMap& mv,
+                          cudaStream_t stream) {
+  if (head_dim != 128) return PKV_ERR_GEOMETRY;
+  switch (block_size) {
+    case 8: return launch_prefill_tc_g<T, 128, 8, true>(p, num_seqs, group, mk, mv, stream);
+    case 16: return launch_prefill_tc_g<T, 128, 16, true>(p, num_seqs, group, mk, mv, stream);
+    case 32: return launch_prefill_tc_g<T, 128, 32, true>(p, num_seqs, group, mk, mv, stream);
+    case 64: return launch_prefill_tc_g<T, 128, 64, true>(p, num_seqs, group, mk, mv, stream);
   }
   return PKV_ERR_GEOMETRY;
 }

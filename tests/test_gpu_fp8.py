@@ -10,7 +10,7 @@ import torch
 import paged_kv_cache_145_gb300 as pkv
 from oracle import attention as A
 from paged_kv_cache_145_gb300 import synth
-from tests.workload import TOL, edge_tol, gpu_out_f64
+from tests.workload import TOL, edge_tol, fp8_tol, gpu_out_f64
 
 pytestmark = pytest.mark.gpu
 IO = {"f16": torch.float16, "bf16": torch.bfloat16}
@@ -144,13 +144,74 @@ def test_fp8_copy_and_swap_are_byte_moves():
     assert np.array_equal(synth.storage_numpy(hv_, "e4m3")[3], ev[2])
 
 
-def test_fp8_prefill_is_refused():
+def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=None, nan_tail=False):
+    lens = [p_ + c for p_, c in zip(prefix, chunk)]
+    nblk = [-(-L // b) for L in lens]
+    n = sum(nblk) + 3
+    cache = fp8_cache(n, hk, b, 128, io, seed, k_scale=k_scale)
+    perm = np.random.default_rng(seed).permutation(n)
+    tables = np.full((len(lens), max(nblk) + 1), -1, dtype=np.int32)
+    pos = 0
+    for i, k in enumerate(nblk):
+        tables[i, :k] = perm[pos:pos + k]
+        pos += k
+    if nan_tail:  # NaN codes in the slots past each sequence's end
+        codes = cache.k_cache.view(torch.uint8), cache.v_cache.view(torch.uint8)
+        for i, L in enumerate(lens):
+            last = int(tables[i, (L - 1) // b])
+            for c in codes:
+                c[last, :, (L - 1) % b + 1:] = 0x7F
+    starts = np.concatenate([[0], np.cumsum(chunk)]).astype(np.int32)
+    q = torch.randn(int(starts[-1]), hk * G, 128, generator=torch.Generator().manual_seed(seed + 5))
+    if q_mult is not None:
+        q = q * q_mult
+    q = q.to(IO[io])
+    scale = 1 / np.sqrt(128)
+    out = pkv.paged_attention_prefill(cache, q.cuda(), torch.from_numpy(starts).cuda(),
+                                      torch.from_numpy(tables).cuda(),
+                                      torch.tensor(lens, dtype=torch.int32).cuda(), scale, max(chunk))
+    assert pkv.paged_get_device_error() == 0
+    ref = A.prefill_attention(synth.storage_numpy(q, io), synth.storage_numpy(cache.k_cache, "e4m3"),
+                              synth.storage_numpy(cache.v_cache, "e4m3"), [list(r) for r in tables],
+                              lens, starts, scale, b, "e4m3", q_dtype=io,
+                              k_scale=cache.k_scale.cpu().numpy(), v_scale=cache.v_scale.cpu().numpy())
+    v_max = float(np.nanmax(np.abs(A.dequantize_pool(synth.storage_numpy(cache.v_cache, "e4m3"),
+                                           cache.v_scale.cpu().numpy()))))
+    return gpu_out_f64(out), ref, v_max
+
+
+@pytest.mark.parametrize("io,G,b", [("f16", 4, 16), ("bf16", 4, 16), ("bf16", 1, 8), ("f16", 8, 64),
+                                    ("bf16", 2, 32)])
+def test_fp8_prefill_matches_oracle(io, G, b):
+    got, ref, vmax = fp8_prefill_case(io, G, b, [0, 5, 100, 17], [37, 64, 3, 130], seed=31 + G + b)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= fp8_tol(io, ref, vmax))
+
+
+def test_fp8_prefill_bf16_queries_beyond_fp16_range():
+    got, ref, vmax = fp8_prefill_case("bf16", 4, 16, [20, 0], [50, 70], seed=43, q_mult=1e5,
+                                      k_scale=torch.full((2,), 3e-7))
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= fp8_tol("bf16", ref, vmax))
+
+
+def test_fp8_prefill_stale_nan_codes():
+    got, ref, vmax = fp8_prefill_case("f16", 4, 16, [3, 0, 40], [5, 17, 9], seed=47, nan_tail=True)
+    assert np.all(np.isfinite(got)) and np.all(np.abs(got - ref) <= fp8_tol("f16", ref, vmax))
+
+
+def test_fp8_prefill_refusals(monkeypatch):
+    # head_dim 64 and the mma.sync prefill kernel do not take FP8 pools.
     cache = fp8_cache(4, 2, 16, 64, "f16", 41)
     q = torch.zeros(3, 2, 64, dtype=torch.float16).cuda()
+    args = (torch.tensor([0, 3], dtype=torch.int32).cuda(), torch.zeros(1, 1, dtype=torch.int32).cuda(),
+            torch.tensor([3], dtype=torch.int32).cuda(), 0.1, 3)
     with pytest.raises(RuntimeError):
-        pkv.paged_attention_prefill(cache, q, torch.tensor([0, 3], dtype=torch.int32).cuda(),
-                                    torch.zeros(1, 1, dtype=torch.int32).cuda(),
-                                    torch.tensor([3], dtype=torch.int32).cuda(), 0.1, 3)
+        pkv.paged_attention_prefill(cache, q, *args)
+    monkeypatch.setenv("PKV_PREFILL_KERNEL", "mma")
+    cache = fp8_cache(4, 2, 16, 128, "f16", 41)
+    with pytest.raises(RuntimeError):
+        pkv.paged_attention_prefill(cache, torch.zeros(3, 2, 128, dtype=torch.float16).cuda(), *args)
 
 
 def test_fp8_default_partition_follows_grid_size():

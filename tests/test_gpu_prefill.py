@@ -163,3 +163,12 @@ def test_prefill_invalid_inputs_zero_rows():
     # A chunk longer than the declared bound is refused on the device too.
     out, err = c.gpu(max_queries=3)
     assert err == pkv.PKV_DEV_SEQ_LEN and np.all(gpu_out_f64(out) == 0)
+
+
+def test_prefill_negative_scale():
+    c = PCase("bf16", 8, 2, 128, 16, [0, 30], [70, 9], seed=9)
+    c.scale = -c.scale
+    out, err = c.gpu()
+    assert err == 0
+    got, ref = gpu_out_f64(out), c.oracle()
+    assert np.all(np.abs(got - ref) <= edge_tol("bf16", ref))
