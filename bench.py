@@ -698,8 +698,17 @@ def run_prefill(args):
     width = max(bm.num_seq_blocks(i) for i in range(S))
     tables, lens = bm.tables(range(S), width)
     seed = synth.seed_of(args.config, 3)
-    cache = pkv.PagedKVCache(synth.normal(seed, (n, Hk, b, D), dt, device="cuda"),
-                             synth.normal(seed + 1, (n, Hk, b, D), dt, device="cuda"))
+    fp8 = args.kv_dtype == "fp8"
+    if fp8:
+        # FP8 E4M3 pool with one scale per KV head (1/64, as for decode): the
+        # step's KV write quantizes the chunk, the prefill reads codes.
+        sc = torch.full((Hk,), 1.0 / 64, dtype=torch.float32, device=dev)
+        cache = pkv.PagedKVCache(synth.random_codes(seed, (n, Hk, b, D), device="cuda"),
+                                 synth.random_codes(seed + 1, (n, Hk, b, D), device="cuda"),
+                                 sc, sc.clone(), synth.TORCH_DTYPE[dt])
+    else:
+        cache = pkv.PagedKVCache(synth.normal(seed, (n, Hk, b, D), dt, device="cuda"),
+                                 synth.normal(seed + 1, (n, Hk, b, D), dt, device="cuda"))
     T = S * chunk
     q = synth.normal(seed + 2, (T, H, D), dt, device="cuda")
     k = synth.normal(seed + 3, (T, Hk, D), dt, device="cuda")
@@ -755,9 +764,10 @@ def run_prefill(args):
         "metric": "paged prefill attention TFLOP/s (causal, GQA)", "value": round(flops / step_s / 1e12, 3),
         "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(step_s * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "vs_baseline": None, "dtype": dt if not fp8 else "%s (KV cache e4m3, fp16 MMAs)" % dt,
+        "data": "synthetic",
         "config": {"workload": args.config, "about": cfg["about"], "sequences": S, "prefix": prefix,
-                   "chunk": chunk, "pool_blocks": n},
+                   "chunk": chunk, "pool_blocks": n, "kv_dtype": "e4m3" if fp8 else dt},
         "prefill_tokens_per_s": round(T / step_s, 1),
         "roofline": {"bound": "tensor", "achieved": round(flops / attn_s / 1e12, 2), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(flops / attn_s / 1e12 / peak, 4), "traffic": None,

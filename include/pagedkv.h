@@ -208,10 +208,14 @@ int paged_attention_decode(const pkv_cache* cache, const void* q,
  * chunk sits at position L - Q + i and attends to positions 0 .. L - Q + i:
  *     out[query_starts[s] + i][h] = softmax-weighted mean, as in
  *     paged_attention_decode, over the first L - Q + i + 1 positions
- * accumulated in float32 on tensor cores.  fp16 and bf16 pools only (not
- * FP8).
+ * accumulated in float32 on tensor cores.  fp16, bf16 and FP8 pools; FP8
+ * pools with head_dim 128 only (others: PKV_ERR_GEOMETRY), their keys and
+ * values being the codes' values times the head's scales, with q and out in
+ * io_dtype.  PKV_PREFILL_KERNEL=mma in the environment selects the mma.sync
+ * kernel (16-bit pools only).
  *
  *   q, out        device, [total_queries][num_heads][head_dim], cache dtype
+ *                 (io_dtype for FP8 pools)
  *   query_starts  device, int32[num_seqs + 1], non-decreasing, last <=
  *                 total_queries
  *   max_queries   host bound on any sequence's Q (sizes the launch)
