@@ -50,19 +50,19 @@ from paged_kv_cache_145_gb300 import synth  # noqa: E402
 METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
 
 # DRAM bytes (read + write) per launch of the decode partition kernel, from
-# ncu (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload and
-# KV dtype, with the hash of the sources of that kernel family they were
-# taken on.  A stale hash reports null.
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, KV
+# dtype and partition length, with the hash of the sources of that kernel
+# family they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b": (1280424472, "118000bf3980d6e6"),
-    "gqa": (1129142640, "118000bf3980d6e6"),
-    "opt13b/fp8": (644210176, "1ba078747bf5507f"),
-    "gqa/fp8": (565904896, "1ba078747bf5507f"),
+    "opt13b/native/512": (1280424472, "118000bf3980d6e6"),
+    "gqa/native/512": (1129142640, "118000bf3980d6e6"),
+    "opt13b/fp8/2048": (644210176, "a67ff3c59e9fdaf1"),
+    "gqa/fp8/2048": (565904896, "a67ff3c59e9fdaf1"),
 }
 
 KERNEL_SOURCES = {
     "native": ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh"),
-    "fp8": ("common.cuh", "decode.cuh", "decode_mma_fp8.cuh", "decode_launch.cuh", "api.cu"),
+    "fp8": ("common.cuh", "decode.cuh", "decode_mma_fp8.cuh", "decode_launch.cuh"),
 }
 
 
@@ -586,7 +586,8 @@ def run_ours(args):
     layers = w.cfg.get("layers", 1)
     src_hash = kernel_source_hash("fp8" if kv_dtype else "native")
     default_shape = args.partition == 0 and args.block_size == 0 and args.table == "shuffled"
-    tr = TRAFFIC.get(args.config + ("/fp8" if kv_dtype else "")) if default_shape else None
+    key = "%s/%s/%d" % (args.config, "fp8" if kv_dtype else "native", part)
+    tr = TRAFFIC.get(key) if default_shape else None
     traffic = tr[0] if tr and tr[1] == src_hash else None
     line = {
         "metric": METRIC,

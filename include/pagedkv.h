@@ -123,11 +123,11 @@ int paged_kv_write(const pkv_cache* cache, const void* k, const void* v,
 /*
  * paged_attention_partition_size -- the partition length (in positions) a
  * decode call will use.  `requested` = 0 selects the library default:
- * 512 for 16- and 32-bit pools; for FP8 pools the longest of 2048, 1024
- * and 512 for which num_seqs * num_kv_heads * ceil(max_seq_len / length)
- * reaches 12 thread blocks per SM of the current device.  Otherwise it must
- * be a positive multiple of block_size no larger than 8192 and is returned
- * unchanged.  Returns a negative PKV_ERR_* on bad arguments.  The default
+ * 512 for 16- and 32-bit pools; for FP8 pools the longest of 2048, 1536,
+ * 1024 and 512 for which num_seqs * num_kv_heads * ceil(max_seq_len /
+ * length) reaches 8 thread blocks per SM of the current device.
+ * Otherwise it must be a positive multiple of block_size no larger than
+ * 8192 and is returned unchanged.  Returns a negative PKV_ERR_* on bad arguments.  The default
  * depends on (num_seqs, max_seq_len): size the workspace and call decode
  * with the same values.
  */

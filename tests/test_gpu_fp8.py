@@ -215,14 +215,14 @@ def test_fp8_prefill_refusals(monkeypatch):
 
 
 def test_fp8_default_partition_follows_grid_size():
-    """FP8 pools default to the longest of 2048 / 1024 / 512 positions that
-    still launches 12 thread blocks per SM; 16-bit pools keep 512."""
+    """FP8 pools default to the longest of 2048 / 1536 / 1024 / 512 positions
+    that still launches 8 thread blocks per SM; 16-bit pools keep 512."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     cache = fp8_cache(4, 8, 16, 128, "bf16", 5)
 
     def expect(S, L):
-        for part in (2048, 1024):
-            if S * 8 * -(-L // part) >= 12 * sms:
+        for part in (2048, 1536, 1024):
+            if S * 8 * -(-L // part) >= 8 * sms:
                 return part
         return 512
 
