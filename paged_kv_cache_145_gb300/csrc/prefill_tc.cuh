@@ -1,5 +1,6 @@
 // Paged causal prefill attention on the fifth-generation tensor cores
-// (tcgen05, accumulators in tensor memory), fp16 / bf16 pools.
+// (tcgen05, accumulators in tensor memory), fp16 / bf16 pools and FP8 E4M3
+// pools (head_dim 128).
 //
 // Same operation as prefill_mma_kernel ("vLLM and PagedAttention: Virtual
 // Memory for LLM Serving", opening paragraph; "Inside vLLM and TGI: Paging,
@@ -27,7 +28,12 @@
 //              memory in MN-major form, 128 x D x 64).  S_t(j+1) is issued as
 //              soon as the softmax has read S_t(j), P.V_t(j) once P_t(j) is
 //              written; each issuer zeroes the value rows past the last
-//              needed key before its last P.V.
+//              needed key before its last P.V;
+//   warps 11-14 (FP8 pools only) converters: widen the producer's raw code
+//              tiles into the fp16 operand tiles (exact), writing zeros for
+//              value rows past the last needed key.  Both products then run
+//              in fp16 with P unsplit; bf16 queries enter as fp16 with a
+//              per-row power-of-two shift.
 // The running maximum is raised lazily: O and the sum are rescaled only
 // when a row's maximum grows by more than 2^8, so P stays at or below 256
 // and most tiles skip the tensor-memory round trip of O.
