@@ -322,6 +322,17 @@ int paged_block_swap(const pkv_cache* cache, void* host_k, void* host_v, int64_t
  */
 int paged_get_device_error(cudaStream_t stream, uint32_t* bits);
 
+/*
+ * paged_selftest_wait_timeout -- exercises the failure path every kernel
+ * shares.  The pages have no counterpart.  A one-warp kernel waits on a
+ * barrier that nothing completes; after limit_ns nanoseconds of wall-clock
+ * time (1 .. 10^9) the bounded wait gives up, sets PKV_DEV_TIMEOUT in the
+ * device error word and returns, as any kernel's copy wait would.  Nothing
+ * faults and the context stays usable.  PKV_ERR_ARG for a limit outside
+ * the range.
+ */
+int paged_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
 /* Text for a PKV_ERR_* code. */
 const char* paged_strerror(int code);
 

@@ -28,7 +28,8 @@ __all__ = [
     "PagedKVCache", "BlockManager", "paged_kv_write", "paged_attention_decode",
     "paged_attention_prefill",
     "paged_attention_workspace_bytes", "paged_attention_partition_size",
-    "paged_block_copy", "paged_block_swap", "paged_get_device_error", "library_path",
+    "paged_block_copy", "paged_block_swap", "paged_get_device_error",
+    "paged_selftest_wait_timeout", "library_path",
 ]
 
 
@@ -237,6 +238,14 @@ def paged_get_device_error(stream=None):
     _lib.check(_lib.lib().paged_get_device_error(_stream(stream), ctypes.byref(bits)),
                "paged_get_device_error")
     return int(bits.value)
+
+
+def paged_selftest_wait_timeout(limit_ns=10_000_000, stream=None):
+    """Run the bounded-wait self-test: a wait that nothing completes gives up
+    after ``limit_ns`` and sets PKV_DEV_TIMEOUT (read it with
+    :func:`paged_get_device_error`)."""
+    _lib.check(_lib.lib().paged_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+               "paged_selftest_wait_timeout")
 
 
 def _i64(a):
