@@ -75,8 +75,11 @@ struct PrefillTcCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;     // one Q tile (128 rows)
   static constexpr int kKvHalfBytes = kKeys * 128;               // 64 key rows x 128 B
   static constexpr int kKvBytes = kHalves * kKvHalfBytes;        // one K or V tile
+  // Operand (K/V) ring; FP8 pools add a raw-code ring.  FP8, measured on the
+  // 2048-token prompt / chunked workloads (operand x raw stages, TFLOP/s):
+  // 2 x 4 628 / 745, 3 x 2 701 / 874, 3 x 3 668 / 867, 4 x 2 665 / 861.
   static constexpr int kStages =
-      KV8 ? 2 : (QT == 2 ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 2));  // widened K/V ring
+      KV8 ? 3 : (QT == 2 ? (D == 64 ? 6 : 4) : (D == 64 ? 4 : 2));
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
   static constexpr int kBoxes = kKeys / kBoxRows;  // TMA boxes per tile per column block
   static constexpr int kSoftmaxWarps = 4 * QT;
@@ -91,7 +94,7 @@ struct PrefillTcCfg {
   static constexpr int kRingOff = QT * kTileBytes;
   static constexpr int kStageBytes = 2 * kKvBytes;  // K then V
   // FP8 pools: raw code tiles (64 rows x D codes, 128-byte swizzle), K then V.
-  static constexpr int kRawStages = KV8 ? 4 : 0;
+  static constexpr int kRawStages = KV8 ? 2 : 0;
   static constexpr int kRawBytes = kKeys * D;
   static constexpr int kRawOff = kRingOff + kStages * kStageBytes;
   static constexpr int kBarOff = kRawOff + kRawStages * 2 * kRawBytes;
