@@ -1,0 +1,8 @@
+// Prefill attention (tcgen05 kernel) instantiations for bf16 pools.
+#include "prefill_tc.cuh"
+
+int pkv_launch_prefill_tc_bf16(const pkv::PrefillParams& p, int num_seqs, int head_dim,
+                            int block_size, int group, const CUtensorMap& mk,
+                            const CUtensorMap& mv, cudaStream_t stream) {
+  return pkv::launch_prefill_tc<__nv_bfloat16>(p, num_seqs, head_dim, block_size, group, mk, mv, stream);
+}
