@@ -391,6 +391,115 @@ def oracle_timed(name, budget_s, seed=4242):
     return oracle_child(_oracle_sample, name, budget_s, seed)
 
 
+def _oracle_prefill_sample(name, budget_s, seed, fp8):
+    """Times the oracle's chunk write + causal prefill attention over the
+    workload's sequences, one (sequence, KV head) pair at a time with that
+    head's query heads, until ``budget_s`` seconds of oracle work have
+    passed.  Each pair gets a private pool of its sequence's blocks, handed
+    out in shuffled order.  Returns (flops, seconds, pairs, queries)."""
+    from oracle import attention as A
+
+    cfg = synth.CONFIGS[name]
+    b, H, Hk, D, dt = cfg["block_size"], cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
+    prefix, chunk, G = cfg["prefix"], cfg["chunk"], H // Hk
+    L = prefix + chunk
+    nblk = -(-L // b)
+    kdt = "e4m3" if fp8 else dt
+    sc = [1.0 / 64]
+    flops_pair = 4 * D * G * sum(prefix + i + 1 for i in range(chunk))
+    flops, spent, pairs = 0, 0.0, 0
+    for s in range(cfg["batch"]):
+        table = synth.free_order(seed + s, nblk)
+        pos = np.arange(prefix, L)
+        slots = table[pos // b] * b + pos % b
+        for kvh in range(Hk):
+            r = seed + 1000 * s + 10 * kvh
+            if fp8:
+                kp = synth.storage_numpy(synth.random_codes(r, (nblk, 1, b, D)), "e4m3")
+                vp = synth.storage_numpy(synth.random_codes(r + 1, (nblk, 1, b, D)), "e4m3")
+            else:
+                kp = synth.storage_numpy(synth.normal(r, (nblk, 1, b, D), dt), dt)
+                vp = synth.storage_numpy(synth.normal(r + 1, (nblk, 1, b, D), dt), dt)
+            kn = synth.storage_numpy(synth.normal(r + 2, (chunk, 1, D), dt), dt)
+            vn = synth.storage_numpy(synth.normal(r + 3, (chunk, 1, D), dt), dt)
+            q = synth.storage_numpy(synth.normal(r + 4, (chunk, G, D), dt), dt)
+            t0 = time.perf_counter()
+            if fp8:
+                kp, vp, _ = A.write_tokens_fp8(kp, vp, kn, vn, slots, b, sc, sc, dt)
+            else:
+                kp, vp, _ = A.write_tokens(kp, vp, kn, vn, slots, b)
+            A.prefill_attention(q, kp, vp, [table], [L], [0, chunk], 1.0 / math.sqrt(D), b, kdt,
+                                q_dtype=dt, k_scale=sc if fp8 else None,
+                                v_scale=sc if fp8 else None)
+            spent += time.perf_counter() - t0
+            flops += flops_pair
+            pairs += 1
+            if spent >= budget_s:
+                return flops, spent, pairs, chunk
+    return flops, spent, pairs, chunk
+
+
+def _oracle_op_sample(name, op, budget_s, seed, block_size=None):
+    """Times the oracle's KV write, block copy or block swap on samples of
+    the workload until ``budget_s`` seconds of oracle work have passed.
+    write: every position of one sequence after another, each into a private
+    pool of its blocks; copy: 256 shuffled disjoint pairs over a 512-block
+    pool per call; swap: 256 blocks out to a host pool and back per call.
+    Returns (algorithmic bytes, seconds, units) with the bytes counted as the
+    GPU line counts them."""
+    from oracle import attention as A
+
+    cfg = synth.CONFIGS[name]
+    b = block_size or cfg["block_size"]
+    Hk, D, dt = cfg["kv_heads"], cfg["head_dim"], cfg["dtype"]
+    elt = synth.ELEM_BYTES[dt]
+    block_bytes = Hk * b * D * elt
+    nbytes, spent, units = 0, 0.0, 0
+    if op == "write":
+        for i, L in enumerate(_lengths(name)):
+            L = int(L)
+            nblk = -(-L // b)
+            table = synth.free_order(seed + i, nblk)
+            t = np.arange(L)
+            slots = table[t // b] * b + t % b
+            kp = synth.storage_numpy(synth.normal(seed + 4 * i, (nblk, Hk, b, D), dt), dt)
+            vp = synth.storage_numpy(synth.normal(seed + 4 * i + 1, (nblk, Hk, b, D), dt), dt)
+            kn = synth.storage_numpy(synth.normal(seed + 4 * i + 2, (L, Hk, D), dt), dt)
+            vn = synth.storage_numpy(synth.normal(seed + 4 * i + 3, (L, Hk, D), dt), dt)
+            t0 = time.perf_counter()
+            A.write_tokens(kp, vp, kn, vn, slots, b)
+            spent += time.perf_counter() - t0
+            nbytes += 2 * 2 * L * Hk * D * elt + 8 * L
+            units += L
+            if spent >= budget_s:
+                break
+        return nbytes, spent, units
+    half = 256
+    kp = synth.storage_numpy(synth.normal(seed, (2 * half, Hk, b, D), dt), dt)
+    vp = synth.storage_numpy(synth.normal(seed + 1, (2 * half, Hk, b, D), dt), dt)
+    perm = synth.free_order(seed + 2, 2 * half)
+    while spent < budget_s:
+        if op == "copy":
+            pairs = np.stack([perm[:half], perm[half:]], 1)
+            t0 = time.perf_counter()
+            A.copy_blocks(kp, vp, pairs)
+            spent += time.perf_counter() - t0
+            nbytes += 2 * 2 * half * block_bytes + 16 * half
+        else:
+            hk = np.zeros((half, Hk, b, D), dtype=kp.dtype)
+            hv = np.zeros_like(hk)
+            out_pairs = np.stack([perm[:half], np.arange(half)], 1)
+            in_pairs = np.stack([np.arange(half), perm[:half]], 1)
+            t0 = time.perf_counter()
+            _, _, hk2, hv2, _ = A.swap_blocks(kp, vp, hk, hv, out_pairs, "out")
+            A.swap_blocks(kp, vp, hk2, hv2, in_pairs, "in")
+            spent += time.perf_counter() - t0
+            # one swap out and one swap in, each moving 2 * half blocks
+            nbytes += 2 * (2 * half * block_bytes + 16 * half)
+        units += half
+    return nbytes, spent, units
+
+
 # ---------------------------------------------------------------------------
 # arms
 # ---------------------------------------------------------------------------
@@ -683,6 +792,11 @@ def run_prefill(args):
     rank, local_rank, world = dist_env()
     if rank != 0:
         return
+    fp8 = args.kv_dtype == "fp8"
+    # The CPU baseline child is spawned before any GPU work.
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_child(_oracle_prefill_sample, args.config, args.cpu_budget, 4242, fp8)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     cfg = synth.CONFIGS[args.config]
@@ -699,7 +813,6 @@ def run_prefill(args):
     width = max(bm.num_seq_blocks(i) for i in range(S))
     tables, lens = bm.tables(range(S), width)
     seed = synth.seed_of(args.config, 3)
-    fp8 = args.kv_dtype == "fp8"
     if fp8:
         # FP8 E4M3 pool with one scale per KV head (1/64, as for decode): the
         # step's KV write quantizes the chunk, the prefill reads codes.
@@ -711,23 +824,26 @@ def run_prefill(args):
         cache = pkv.PagedKVCache(synth.normal(seed, (n, Hk, b, D), dt, device="cuda"),
                                  synth.normal(seed + 1, (n, Hk, b, D), dt, device="cuda"))
     T = S * chunk
-    q = synth.normal(seed + 2, (T, H, D), dt, device="cuda")
-    k = synth.normal(seed + 3, (T, Hk, D), dt, device="cuda")
-    v = synth.normal(seed + 4, (T, Hk, D), dt, device="cuda")
-    out = torch.empty_like(q)
-    sl = torch.from_numpy(slots).to(dev)
-    starts = torch.arange(0, T + 1, chunk, dtype=torch.int32, device=dev)
-    tab = torch.from_numpy(tables).to(dev)
-    ln = torch.from_numpy(lens).to(dev)
+    q_h = synth.normal(seed + 2, (T, H, D), dt).pin_memory()
+    k_h = synth.normal(seed + 3, (T, Hk, D), dt).pin_memory()
+    v_h = synth.normal(seed + 4, (T, Hk, D), dt).pin_memory()
+    sl_h = torch.from_numpy(slots).pin_memory()
+    starts_h = torch.arange(0, T + 1, chunk, dtype=torch.int32).pin_memory()
+    tab_h = torch.from_numpy(tables).pin_memory()
+    ln_h = torch.from_numpy(lens).pin_memory()
+    host = [q_h, k_h, v_h, sl_h, starts_h, tab_h, ln_h]
+    resident = tuple(t.to(dev) for t in host)
+    out = torch.empty_like(resident[0])
+    out_h = torch.empty_like(q_h).pin_memory()
     scale = 1.0 / math.sqrt(D)
     stream = torch.cuda.current_stream()
 
-    def attend():
-        pkv.paged_attention_prefill(cache, q, starts, tab, ln, scale, chunk, out=out)
+    def attend(x=resident):
+        pkv.paged_attention_prefill(cache, x[0], x[4], x[5], x[6], scale, chunk, out=out)
 
-    def step():
-        pkv.paged_kv_write(cache, k, v, sl)
-        attend()
+    def step(x=resident):
+        pkv.paged_kv_write(cache, x[1], x[2], x[3])
+        attend(x)
 
     def span(fn):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -753,6 +869,24 @@ def run_prefill(args):
     assert pkv.paged_get_device_error() == 0
     step_s = steps_ev[0].elapsed_time(steps_ev[1]) / 1e3 / args.steps
     attn_s = attn_ev[0].elapsed_time(attn_ev[1]) / 1e3 / args.steps
+
+    # End to end through the public API with host buffers: the step's inputs
+    # (queries, new keys/values, slots, chunk starts, tables, lengths) staged
+    # in one pinned host buffer cross to HBM in one copy, the step runs on
+    # views of its device twin, and the output is copied back to the host.
+    host_in, dev_in, views = pack_pinned(host, dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        dev_in.copy_(host_in, non_blocking=True)
+        step(views)
+        out_h.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    assert pkv.paged_get_device_error() == 0
+    assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device output"
     # Algorithmic FLOPs: QK^T and PV, 2 * D each, per (query, head, visible key).
     visible = S * sum(prefix + i + 1 for i in range(chunk))
     flops = 4 * D * H * visible
@@ -778,7 +912,18 @@ def run_prefill(args):
                      "peak_source": kind,
                      "attention_us": round(attn_s * 1e6, 2)},
         "clocks": clocks, "gpu_launches": 3 * args.steps,
+        "e2e": {"value": round(flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": host_in.numel(),
+                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
+                "ms_per_step": round(e2e_s * 1e3, 4)},
     }
+    if cpu is not None:
+        cf, cs, cpairs, cq = cpu
+        line["cpu_baseline"] = {
+            "value": round(cf / cs / 1e12, 9), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": "%d (sequence, KV head) pairs of %d x %d, each its %d-token chunk write + "
+                      "causal prefill of %d queries x %d query heads, float64 NumPy oracle, "
+                      "1 BLAS thread, %.1f s" % (cpairs, S, Hk, cq, cq, H // Hk, cs)}
     print(json.dumps(line), flush=True)
 
 
@@ -795,6 +940,11 @@ def run_op(args):
     rank, local_rank, world = dist_env()
     if rank != 0:
         return
+    # The CPU baseline child is spawned before any GPU work.
+    cpu = None
+    if not args.no_cpu_baseline:
+        cpu = oracle_child(_oracle_op_sample, args.config, args.op, args.cpu_budget, 4242,
+                           args.block_size or None)
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = Workload(args.config, block_size=args.block_size or None, table=args.table)
@@ -806,24 +956,44 @@ def run_op(args):
     block_bytes = w.Hk * w.b * w.D * w.elt
     peak, peak_kind = hbm_peak()
     extra = {}
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
     if args.op == "write":
         # Slots of every cached position of every sequence, through its table.
         t = [np.arange(L) for L in w.seq_lens]
         slots = np.concatenate([w.tables[i][ti // w.b].astype(np.int64) * w.b + ti % w.b
                                 for i, ti in enumerate(t)])
         n = len(slots)
-        k = synth.normal(seed + 2, (n, w.Hk, w.D), w.dtype, device="cuda")
-        v = synth.normal(seed + 3, (n, w.Hk, w.D), w.dtype, device="cuda")
-        sl = torch.from_numpy(slots).to(dev)
+        host = [synth.normal(seed + 2, (n, w.Hk, w.D), w.dtype).pin_memory(),
+                synth.normal(seed + 3, (n, w.Hk, w.D), w.dtype).pin_memory(),
+                torch.from_numpy(slots).pin_memory()]
+        k, v, sl = (t.to(dev) for t in host)
         secs = _timed(lambda: pkv.paged_kv_write(cache, k, v, sl), args.steps, args.warmup, stream)
+        # End to end: the new keys, values and slots cross from pinned host
+        # memory in one copy before every write (the result stays in the pool).
+        host_in, dev_in, views = pack_pinned(host, dev)
+
+        def e2e_step():
+            dev_in.copy_(host_in, non_blocking=True)
+            pkv.paged_kv_write(cache, *views)
+        e2e = (_timed(e2e_step, args.steps, args.warmup, stream), host_in.numel(), 0)
         nbytes = 2 * 2 * n * w.Hk * w.D * w.elt + 8 * n
         metric, unit_count, kernel = "paged KV write GB/s (prefill-sized)", n, "kv_write_kernel"
         extra["tokens"] = n
     elif args.op == "copy":
         perm = synth.free_order(seed + 4, w.N)
         half = w.N // 2
-        pairs = torch.from_numpy(np.stack([perm[:half], perm[half:2 * half]], 1)).to(dev)
+        pairs_h = torch.from_numpy(np.stack([perm[:half], perm[half:2 * half]], 1)).pin_memory()
+        pairs = pairs_h.to(dev)
         secs = _timed(lambda: pkv.paged_block_copy(cache, pairs), args.steps, args.warmup, stream)
+        # End to end: the pair list crosses from pinned host memory first.
+        pairs_d = torch.empty_like(pairs)
+
+        def e2e_step():
+            pairs_d.copy_(pairs_h, non_blocking=True)
+            pkv.paged_block_copy(cache, pairs_d)
+        e2e = (_timed(e2e_step, args.steps, args.warmup, stream), pairs_h.numel() * 8, 0)
         nbytes = 2 * 2 * half * block_bytes + 16 * half
         metric, unit_count, kernel = "paged block copy GB/s (half the pool)", half, "block_move_kernel"
         extra["pairs"] = half
@@ -846,6 +1016,9 @@ def run_op(args):
         c_out = _timed(lambda: hbuf.copy_(dbuf, non_blocking=True), args.steps, args.warmup, stream)
         c_in = _timed(lambda: dbuf.copy_(hbuf, non_blocking=True), args.steps, args.warmup, stream)
         secs = (t_out + t_in) / 2
+        # The swap's own launches already move host memory: the pair lists
+        # are the only extra inputs that cross the link end to end.
+        e2e = (secs, 16 * half, 0)
         nbytes = moved + 16 * half
         peak = moved / ((c_out + c_in) / 2) / 1e9
         peak_kind = "measured in this run: contiguous cudaMemcpyAsync of the same bytes"
@@ -853,6 +1026,8 @@ def run_op(args):
         extra.update(swap_out_gbs=round(moved / t_out / 1e9, 2), swap_in_gbs=round(moved / t_in / 1e9, 2),
                      memcpy_d2h_gbs=round(moved / c_out / 1e9, 2), memcpy_h2d_gbs=round(moved / c_in / 1e9, 2),
                      pairs=half)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
     assert pkv.paged_get_device_error() == 0
     achieved = nbytes / secs / 1e9
     line = {
@@ -865,8 +1040,20 @@ def run_op(args):
         "roofline": {"bound": "hbm" if args.op != "swap" else "host-link", "achieved": round(achieved, 2),
                      "peak": round(peak, 2), "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": None, "kernel": kernel, "peak_source": peak_kind},
+        "clocks": clocks,
         "gpu_launches": args.steps * (2 if args.op == "swap" else 1),
+        "e2e": {"value": round(nbytes / e2e[0] / 1e9, 3), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e[1], "d2h_bytes_per_step": e2e[2],
+                "ms_per_step": round(e2e[0] * 1e3, 5)},
     }
+    if cpu is not None:
+        cb, cs, cu = cpu
+        what = {"write": "%d tokens of whole sequences, each into a private pool of its blocks",
+                "copy": "%d pairs, 256 per call over a 512-block pool",
+                "swap": "%d blocks, 256 out to a host pool and back per call"}[args.op] % cu
+        line["cpu_baseline"] = {
+            "value": round(cb / cs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%s, NumPy oracle, 1 thread, %.1f s" % (what, cs)}
     print(json.dumps(line), flush=True)
 
 

@@ -93,3 +93,21 @@ def test_slot_utilization_matches_oracle_closed_form():
             w = bench.Workload("opt13b", block_size=b, table=table)
             lens = [int(x) for x in w.seq_lens]
             assert abs(w.utilization - float(P.paged_utilization(lens, b))) < 1e-12
+
+
+def test_cpu_baseline_samples_count_their_work():
+    # Prefill: one (sequence, KV head) pair of the chunked workload covers
+    # 512 queries x 4 query heads, query i seeing 4096 + i + 1 positions;
+    # QK^T and PV are 2 * 128 FLOPs each per visible position.
+    f, secs, pairs, q = bench._oracle_prefill_sample("chunked", 1e-9, 4242, False)
+    assert pairs == 1 and q == 512 and secs > 0
+    assert f == 4 * 128 * 4 * (512 * 4097 + 511 * 512 // 2)
+    # Data movers: bytes counted as the GPU line counts them.
+    blk = 40 * 16 * 128 * 2
+    b, secs, units = bench._oracle_op_sample("opt13b", "copy", 1e-9, 4242)
+    assert units == 256 and b == 2 * 2 * 256 * blk + 16 * 256
+    b, secs, units = bench._oracle_op_sample("opt13b", "swap", 1e-9, 4242)
+    assert units == 256 and b == 2 * (2 * 256 * blk + 16 * 256)
+    b, secs, units = bench._oracle_op_sample("gqa", "write", 1e-9, 4242)
+    n = int(bench._lengths("gqa")[0])
+    assert units == n and b == 2 * 2 * n * 8 * 128 * 2 + 8 * n
