@@ -58,6 +58,9 @@ TRAFFIC = {
     "gqa/native/512": (1129142640, "118000bf3980d6e6"),
     "opt13b/fp8/2048": (644210176, "a67ff3c59e9fdaf1"),
     "gqa/fp8/2048": (565904896, "a67ff3c59e9fdaf1"),
+    "long/native/512": (877668096, "118000bf3980d6e6"),
+    "long/fp8/1536": (439782912, "a67ff3c59e9fdaf1"),
+    "fork/native/512": (79609344, "118000bf3980d6e6"),
 }
 
 KERNEL_SOURCES = {
