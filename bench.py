@@ -98,6 +98,57 @@ def pack_pinned(tensors, dev, align=256):
     return host, devbuf, views
 
 
+def e2e_pipelined(host_tensors, dev, step, out_like, steps):
+    """End-to-end steps through the public API from pinned host memory.
+
+    Every step's inputs cross the host link in one copy (into one of two
+    device staging buffers, on a host-to-device stream) and its output comes
+    back in one copy (from one of two device outputs, on a device-to-host
+    stream), so step i's copies overlap the kernels of steps i - 1 and
+    i + 1, as a serving loop would stage them.  ``step(views, out)`` runs
+    one step on the current stream.  Returns (seconds per step, h2d bytes
+    per step, d2h bytes per step, the last output copied to the host, the
+    device output it came from)."""
+    import torch
+
+    compute = torch.cuda.current_stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    staged = [pack_pinned(host_tensors, dev) for _ in range(2)]
+    outs = [torch.empty_like(out_like) for _ in range(2)]
+    outs_h = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
+    ev = lambda: torch.cuda.Event()  # noqa: E731
+    ev_in, ev_done, ev_out = [ev(), ev()], [ev(), ev()], [ev(), ev()]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(compute)
+    h2d.wait_stream(compute)
+    d2h.wait_stream(compute)
+    for i in range(steps):
+        k = i % 2
+        host_in, dev_in, views = staged[k]
+        with torch.cuda.stream(h2d):
+            if i >= 2:
+                h2d.wait_event(ev_done[k])  # step i - 2 has read this staging buffer
+            dev_in.copy_(host_in, non_blocking=True)
+            ev_in[k].record(h2d)
+        compute.wait_event(ev_in[k])
+        if i >= 2:
+            compute.wait_event(ev_out[k])  # step i - 2's output has left this buffer
+        step(views, outs[k])
+        ev_done[k].record(compute)
+        with torch.cuda.stream(d2h):
+            d2h.wait_event(ev_done[k])
+            outs_h[k].copy_(outs[k], non_blocking=True)
+            ev_out[k].record(d2h)
+    compute.wait_stream(h2d)
+    compute.wait_stream(d2h)
+    end.record(compute)
+    torch.cuda.synchronize()
+    last = (steps - 1) % 2
+    return (start.elapsed_time(end) / 1e3 / steps, staged[0][0].numel(),
+            outs_h[0].numel() * outs_h[0].element_size(), outs_h[last], outs[last])
+
+
 def hbm_peak():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -592,15 +643,15 @@ def run_ours(args):
 
     resident = (q, k, v, slots, tables, lens, pairs)
 
-    def decode(x=resident):
-        pkv.paged_attention_decode(cache, x[0], x[4], x[5], scale, out=out, max_seq_len=w.max_len,
+    def decode(x=resident, o=out):
+        pkv.paged_attention_decode(cache, x[0], x[4], x[5], scale, out=o, max_seq_len=w.max_len,
                                    workspace=ws, partition_size=part)
 
-    def step(x=resident):
+    def step(x=resident, o=out):
         if has_pairs:
             pkv.paged_block_copy(cache, x[6])
         pkv.paged_kv_write(cache, x[1], x[2], x[3])
-        decode(x)
+        decode(x, o)
 
     for _ in range(args.warmup):
         step()
@@ -657,30 +708,39 @@ def run_ours(args):
     # End to end through the public API with host buffers: the step's inputs
     # (q, new k/v, slots, tables, lengths and copy pairs) staged in one
     # pinned host buffer cross to HBM in one copy, the step runs on views of
-    # its device twin, and the output is copied back to the host.
-    host_in, dev_in, views = pack_pinned([q_h, k_h, v_h, slots_h, tables_h, lens_h, pairs_h], dev)
-    h2d = host_in.numel()
-    d2h = out_h.numel() * out_h.element_size()
+    # its device twin, and the output is copied back to the host.  Without
+    # an L2 flush the copies run on their own streams, overlapping the
+    # neighbouring steps' kernels; with one (a pool that fits in L2) each
+    # step is copied in, run and copied out in turn, timed without the
+    # flushes.
     e2e_steps = args.steps
-    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
-    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+    e2e_inputs = [q_h, k_h, v_h, slots_h, tables_h, lens_h, pairs_h]
     barrier()
-    torch.cuda.synchronize()
-    for i in range(e2e_steps):
-        if flush_l2:
+    if flush_l2:
+        host_in, dev_in, views = pack_pinned(e2e_inputs, dev)
+        h2d = host_in.numel()
+        d2h = out_h.numel() * out_h.element_size()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(e2e_steps)]
+        torch.cuda.synchronize()
+        for i in range(e2e_steps):
             flush_buf.fill_(i & 0xFF)
-        if flush_l2 or i == 0:
             e0[i].record(stream)
-        dev_in.copy_(host_in, non_blocking=True)
-        step(views)
-        out_h.copy_(out, non_blocking=True)
-        if flush_l2 or i == e2e_steps - 1:
+            dev_in.copy_(host_in, non_blocking=True)
+            step(views)
+            out_h.copy_(out, non_blocking=True)
             e1[i].record(stream)
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        e2e_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps))
+        e2e_host, e2e_dev = out_h, out
+        e2e_mode = "serial (L2 flushed between steps)"
+    else:
+        per_step, h2d, d2h, e2e_host, e2e_dev = e2e_pipelined(e2e_inputs, dev, step, out, e2e_steps)
+        e2e_ms = per_step * 1e3 * e2e_steps
+        e2e_mode = "copies on their own streams, overlapping the neighbouring steps"
     barrier()
-    e2e_ms = (sum(e0[i].elapsed_time(e1[i]) for i in range(e2e_steps)) if flush_l2
-              else e0[0].elapsed_time(e1[-1]))
-    assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device output"
+    assert pkv.paged_get_device_error() == 0
+    assert torch.equal(e2e_host, e2e_dev.cpu()), "end-to-end output differs from the device output"
 
     dec_bytes, kv_bytes = w.decode_bytes(part)
     step_bytes = dec_bytes + w.write_bytes() + (w.copy_bytes() if has_pairs else 0)
@@ -744,7 +804,7 @@ def run_ours(args):
         "gpu_launches": (launches_per_step + decode_launches) * args.steps,
         "e2e": {"value": round(all_e2e_bytes / max_e2e_s / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5)},
+                "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5), "copies": e2e_mode},
     }
     if warm is not None:
         line["warm_l2"] = {
@@ -837,16 +897,15 @@ def run_prefill(args):
     host = [q_h, k_h, v_h, sl_h, starts_h, tab_h, ln_h]
     resident = tuple(t.to(dev) for t in host)
     out = torch.empty_like(resident[0])
-    out_h = torch.empty_like(q_h).pin_memory()
     scale = 1.0 / math.sqrt(D)
     stream = torch.cuda.current_stream()
 
-    def attend(x=resident):
-        pkv.paged_attention_prefill(cache, x[0], x[4], x[5], x[6], scale, chunk, out=out)
+    def attend(x=resident, o=out):
+        pkv.paged_attention_prefill(cache, x[0], x[4], x[5], x[6], scale, chunk, out=o)
 
-    def step(x=resident):
+    def step(x=resident, o=out):
         pkv.paged_kv_write(cache, x[1], x[2], x[3])
-        attend(x)
+        attend(x, o)
 
     def span(fn):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -876,20 +935,11 @@ def run_prefill(args):
     # End to end through the public API with host buffers: the step's inputs
     # (queries, new keys/values, slots, chunk starts, tables, lengths) staged
     # in one pinned host buffer cross to HBM in one copy, the step runs on
-    # views of its device twin, and the output is copied back to the host.
-    host_in, dev_in, views = pack_pinned(host, dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(args.steps):
-        dev_in.copy_(host_in, non_blocking=True)
-        step(views)
-        out_h.copy_(out, non_blocking=True)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_s = e0.elapsed_time(e1) / 1e3 / args.steps
+    # views of its device twin, and the output is copied back to the host,
+    # the copies on their own streams overlapping the neighbouring steps.
+    e2e_s, h2d, d2h, e2e_host, e2e_dev = e2e_pipelined(host, dev, step, out, args.steps)
     assert pkv.paged_get_device_error() == 0
-    assert torch.equal(out_h, out.cpu()), "end-to-end output differs from the device output"
+    assert torch.equal(e2e_host, e2e_dev.cpu()), "end-to-end output differs from the device output"
     # Algorithmic FLOPs: QK^T and PV, 2 * D each, per (query, head, visible key).
     visible = S * sum(prefix + i + 1 for i in range(chunk))
     flops = 4 * D * H * visible
@@ -916,9 +966,9 @@ def run_prefill(args):
                      "attention_us": round(attn_s * 1e6, 2)},
         "clocks": clocks, "gpu_launches": 3 * args.steps,
         "e2e": {"value": round(flops / e2e_s / 1e12, 3), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": host_in.numel(),
-                "d2h_bytes_per_step": out_h.numel() * out_h.element_size(),
-                "ms_per_step": round(e2e_s * 1e3, 4)},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4),
+                "copies": "copies on their own streams, overlapping the neighbouring steps"},
     }
     if cpu is not None:
         cf, cs, cpairs, cq = cpu
