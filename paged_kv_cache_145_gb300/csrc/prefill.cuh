@@ -45,6 +45,12 @@ struct PrefillParams {
   unsigned* err;
   const float* k_scale;    // FP8 pools: [Hk] key / value scales (else unused)
   const float* v_scale;
+  // tcgen05 kernel only (1-D grid of work items, heaviest query tiles
+  // first): query tiles per sequence, sequences, and the number of items
+  // that run whole; each later item runs as two CTAs of one Q tile each.
+  int q_tiles;
+  int num_seqs;
+  int n_full;
 };
 
 template <typename T, int D, int BS, int G>

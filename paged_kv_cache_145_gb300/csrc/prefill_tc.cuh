@@ -178,9 +178,19 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                                     (Cfg::kAlign - 1));
   const uint32_t sbase = smem_addr(smem);
 
-  const int tile = gridDim.x - 1 - blockIdx.x;  // heaviest tiles first
-  const int kvh = blockIdx.y;
-  const int s = blockIdx.z;
+  // Work item: query tiles heaviest first, each over every (KV head,
+  // sequence).  Items from n_full on run as two CTAs, one per Q tile
+  // (half = 0 or 1), so that the last wave of CTAs ends sooner.
+  int item = blockIdx.x, half = -1;
+  if (item >= p.n_full) {
+    half = (item - p.n_full) & 1;
+    item = p.n_full + ((item - p.n_full) >> 1);
+  }
+  const int pairs = p.kv_heads * p.num_seqs;
+  const int tile = p.q_tiles - 1 - item / pairs;
+  const int kvh = (item % pairs) % p.kv_heads;
+  const int s = (item % pairs) / p.kv_heads;
+  auto active = [&](int t) { return half < 0 || t == half; };
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.num_heads;
@@ -197,6 +207,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   const int qa = tile * Cfg::kQueries;
   if (qa >= Q) return;
   const int qend = min(Q, qa + Cfg::kQueries);
+  // Queries of the active rows: Q tile 0 holds rows 0..127 (queries
+  // qa .. qa + kQueries / 2 - 1), tile 1 the rest.
+  const int qlo = half == 1 ? qa + Cfg::kQueries / 2 : qa;
+  const int qhi = half == 0 ? min(Q, qa + Cfg::kQueries / 2) : qend;
+  if (qlo >= qhi) return;  // a second half with no real query
   auto zero_rows = [&]() {
     for (int e = threadIdx.x; e < (qend - qa) * G * D; e += Cfg::kThreads) {
       const int qi = qa + e / (G * D);
@@ -209,8 +224,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
     zero_rows();
     return;
   }
-  const int first = L - Q;          // position of query 0
-  const int n_keys = first + qend;  // keys 0 .. n_keys-1 are visible to some row
+  const int first = L - Q;         // position of query 0
+  const int n_keys = first + qhi;  // keys 0 .. n_keys-1 are visible to some active row
   const int nblk = (n_keys + BS - 1) / BS;
   const int n_tiles = (n_keys + KT - 1) / KT;
   const int32_t* trow = p.tables + (int64_t)s * p.max_blocks;
@@ -246,7 +261,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       // every converter thread arrives once it has widened its part.
       mbar_init(k_full(st), KV8 ? Cfg::kConvThreads : 1);
       mbar_init(v_full(st), KV8 ? Cfg::kConvThreads : 1);
-      mbar_init(kv_empty(st), QT);  // every Q tile's P.V
+      mbar_init(kv_empty(st), half < 0 ? QT : 1);  // every active Q tile's P.V
     }
     for (int t = 0; t < QT; ++t) {
       mbar_init(s_full(t), 1);
@@ -277,7 +292,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   const int R = t * Cfg::kTileRows + rr;
   const int qi = min(qa + R / G, Q - 1);
   float row_scale = 1.f;  // FP8 pools: this row's factor on its scores
-  if (warp < Cfg::kSoftmaxWarps) {
+  if (warp < Cfg::kSoftmaxWarps && active(t)) {
     const uint4* qrow = reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) +
                                                        ((int64_t)(q0 + qi) * H + kvh * G + R % G) * D);
     unsigned char* qt = smem + Cfg::kQOff + t * Cfg::kTileBytes;
@@ -397,6 +412,9 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         mbar_wait(v_full(j % RING), (uint32_t)((j / RING) & 1), kWaitLimitNs / 8);
       }
     }
+  } else if (warp >= Cfg::kMmaWarp && warp < Cfg::kMmaWarp + QT &&
+             !active(warp - Cfg::kMmaWarp)) {
+    // The issuer of a Q tile this CTA does not run has nothing to do.
   } else if (warp >= Cfg::kMmaWarp && warp < Cfg::kMmaWarp + QT) {
     // ---- MMA issuers, one per Q tile t: S_t(0); then per K/V tile j:
     //      S_t(j+1) once the softmax has read S_t(j), and P.V_t(j) once
@@ -533,6 +551,8 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
       }
       mbar_arrive(raw_empty(rs));
     }
+  } else if (!active(t)) {
+    // Softmax warps of a Q tile this CTA does not run have nothing to do.
   } else {
     // ---- softmax, row rr of Q tile t ----------------------------------------
     const int pos = first + qi;
@@ -704,9 +724,26 @@ int launch_prefill_tc_cfg(const PrefillParams& p, int num_seqs, const CUtensorMa
       return PKV_ERR_CUDA;
     ready.fetch_or(bit);
   }
-  dim3 grid((unsigned)((p.max_queries + Cfg::kQueries - 1) / Cfg::kQueries), (unsigned)p.kv_heads,
-            (unsigned)num_seqs);
-  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, mk, mv);
+  // One CTA per SM.  When the last wave would hold at most half the SMs'
+  // worth of items, those items (the lightest: query tiles run heaviest
+  // first) each run as two CTAs of one Q tile, which fill the idle SMs and
+  // end the wave in about half the time.
+  static std::atomic<int> sm_count[64];
+  int sms = sm_count[dev & 63].load();
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return PKV_ERR_CUDA;
+    sm_count[dev & 63].store(sms);
+  }
+  PrefillParams q = p;
+  q.q_tiles = (p.max_queries + Cfg::kQueries - 1) / Cfg::kQueries;
+  q.num_seqs = num_seqs;
+  const int64_t items = (int64_t)q.q_tiles * p.kv_heads * num_seqs;
+  const int64_t rem = items % sms;
+  const int64_t split = (rem > 0 && 2 * rem <= sms) ? rem : 0;
+  if (items + split > 0x7FFFFFFF) return PKV_ERR_GEOMETRY;
+  q.n_full = (int)(items - split);
+  kern<<<(unsigned)(items + split), Cfg::kThreads, Cfg::kSmemBytes, stream>>>(q, mk, mv);
   return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

@@ -144,7 +144,8 @@ def test_fp8_copy_and_swap_are_byte_moves():
     assert np.array_equal(synth.storage_numpy(hv_, "e4m3")[3], ev[2])
 
 
-def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=None, nan_tail=False):
+def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=None, nan_tail=False,
+                     seqs=None):
     lens = [p_ + c for p_, c in zip(prefix, chunk)]
     nblk = [-(-L // b) for L in lens]
     n = sum(nblk) + 3
@@ -173,7 +174,7 @@ def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=N
     assert pkv.paged_get_device_error() == 0
     ref = A.prefill_attention(synth.storage_numpy(q, io), synth.storage_numpy(cache.k_cache, "e4m3"),
                               synth.storage_numpy(cache.v_cache, "e4m3"), [list(r) for r in tables],
-                              lens, starts, scale, b, "e4m3", q_dtype=io,
+                              lens, starts, scale, b, "e4m3", seqs=seqs, q_dtype=io,
                               k_scale=cache.k_scale.cpu().numpy(), v_scale=cache.v_scale.cpu().numpy())
     v_max = float(np.nanmax(np.abs(A.dequantize_pool(synth.storage_numpy(cache.v_cache, "e4m3"),
                                            cache.v_scale.cpu().numpy()))))
@@ -186,6 +187,20 @@ def test_fp8_prefill_matches_oracle(io, G, b):
     got, ref, vmax = fp8_prefill_case(io, G, b, [0, 5, 100, 17], [37, 64, 3, 130], seed=31 + G + b)
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= fp8_tol(io, ref, vmax))
+
+
+def test_fp8_prefill_chunked_workload_full_size_sampled():
+    # The benchmark's FP8 chunked-prefill workload at full size (8 x (4096
+    # cached + 512 queries), GQA 32/8, bf16 I/O, block 16), in its launch
+    # configuration; two whole sequences against the oracle.
+    cfg = synth.CONFIGS["chunked"]
+    S, G = cfg["batch"], cfg["heads"] // cfg["kv_heads"]
+    chunk = [cfg["chunk"]] * S
+    got, ref, vmax = fp8_prefill_case("bf16", G, cfg["block_size"], [cfg["prefix"]] * S, chunk,
+                                      seed=47, hk=cfg["kv_heads"], seqs=[0, S - 1])
+    assert np.all(np.isfinite(got))
+    rows = np.concatenate([np.arange(0, chunk[0]), np.arange(sum(chunk) - chunk[-1], sum(chunk))])
+    assert np.all(np.abs(got[rows] - ref[rows]) <= fp8_tol("bf16", ref[rows], vmax))
 
 
 def test_fp8_prefill_bf16_queries_beyond_fp16_range():

@@ -85,6 +85,26 @@ def test_prefill_geometry_grid(dt, D, b, G):
     assert np.all(np.abs(got - ref) <= edge_tol(dt, ref))
 
 
+def test_prefill_chunked_workload_full_size_sampled():
+    # The benchmark's chunked-prefill workload at full size (8 sequences of
+    # 4096 cached positions and a 512-query chunk, GQA 32/8, bf16, block 16)
+    # in the launch configuration the benchmark times: 512 query tiles, so
+    # on a GPU whose SM count leaves a short last wave the lightest tiles
+    # run as two half CTAs.  Two whole sequences against the oracle.
+    cfg = synth.CONFIGS["chunked"]
+    S = cfg["batch"]
+    c = PCase("bf16", cfg["heads"], cfg["kv_heads"], cfg["head_dim"], cfg["block_size"],
+              [cfg["prefix"]] * S, [cfg["chunk"]] * S, seed=17)
+    out, err = c.gpu()
+    assert err == 0
+    got = gpu_out_f64(out)
+    assert np.all(np.isfinite(got))
+    seqs = [0, S - 1]
+    ref = c.oracle(seqs=seqs)
+    rows = np.concatenate([np.arange(c.starts[s], c.starts[s + 1]) for s in seqs])
+    assert np.all(np.abs(got[rows] - ref[rows]) <= edge_tol("bf16", ref[rows]))
+
+
 def test_prefill_chunked_flow_through_block_manager():
     # Prefix of 300 cached positions per sequence, then a 64-query chunk:
     # the native block manager extends each table and names the chunk's
