@@ -9,11 +9,14 @@
 // query i sits at position L - Q + i and attends to positions 0 .. L - Q + i
 // through the block table.
 //
-// Work decomposition (this library's design): one CTA per (query tile, KV
-// head, sequence).  A CTA holds two Q tiles, A and B, of 128 rows each; a
-// row is a (query, grouped head) pair, so the G query heads sharing a KV
-// head share every K/V tile.  Keys stream in tiles of 64 positions.  Eleven
-// warps with fixed roles:
+// Work decomposition (this library's design): one work item per (query
+// tile, KV head, sequence), on a 1-D grid with the heaviest query tiles
+// first.  An item holds two Q tiles, A and B, of 128 rows each; a row is a
+// (query, grouped head) pair, so the G query heads sharing a KV head share
+// every K/V tile.  One CTA runs an item, except that when the last wave of
+// CTAs would leave at least half the SMs idle, its items run as two CTAs of
+// one Q tile each.  Keys stream in tiles of 64 positions.  Eleven warps
+// with fixed roles:
 //   warps 0-7  softmax: warp w serves Q tile w / 4; thread = one row = one
 //              tensor-memory lane: loads its S row, releases S, masks keys
 //              past its position, keeps the running maximum and sum, writes
