@@ -45,11 +45,13 @@ struct PrefillParams {
   unsigned* err;
   const float* k_scale;    // FP8 pools: [Hk] key / value scales (else unused)
   const float* v_scale;
-  // tcgen05 kernel only (1-D grid of work items, heaviest query tiles
-  // first): query tiles per sequence, sequences, and the number of items
-  // that run whole; each later item runs as two CTAs of one Q tile each.
+  // tcgen05 kernel only (1-D grid of work items): query tiles per sequence,
+  // sequences, (KV head, sequence) pairs per group (items run group by
+  // group, heaviest query tiles first within a group), and the number of
+  // items that run whole; each later item runs as two CTAs of one Q tile.
   int q_tiles;
   int num_seqs;
+  int group_pairs;
   int n_full;
 };
 

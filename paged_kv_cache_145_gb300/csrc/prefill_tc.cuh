@@ -47,6 +47,7 @@
 // the tensor memory is released on every path.
 #pragma once
 
+#include <algorithm>
 #include <type_traits>
 
 #include "decode_mma_fp8.cuh"
@@ -181,18 +182,24 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
                                     (Cfg::kAlign - 1));
   const uint32_t sbase = smem_addr(smem);
 
-  // Work item: query tiles heaviest first, each over every (KV head,
-  // sequence).  Items from n_full on run as two CTAs, one per Q tile
-  // (half = 0 or 1), so that the last wave of CTAs ends sooner.
+  // Work item: the (KV head, sequence) pairs run in groups of group_pairs,
+  // small enough that a group's K/V pages stay in L2 while its CTAs read
+  // them; within a group, query tiles heaviest first over every pair.
+  // Items from n_full on run as two CTAs, one per Q tile (half = 0 or 1),
+  // so that the last wave of CTAs ends sooner.
   int item = blockIdx.x, half = -1;
   if (item >= p.n_full) {
     half = (item - p.n_full) & 1;
     item = p.n_full + ((item - p.n_full) >> 1);
   }
   const int pairs = p.kv_heads * p.num_seqs;
-  const int tile = p.q_tiles - 1 - item / pairs;
-  const int kvh = (item % pairs) % p.kv_heads;
-  const int s = (item % pairs) / p.kv_heads;
+  const int group = item / (p.group_pairs * p.q_tiles);
+  const int in_group = item % (p.group_pairs * p.q_tiles);
+  const int gpairs = min(p.group_pairs, pairs - group * p.group_pairs);
+  const int tile = p.q_tiles - 1 - in_group / gpairs;
+  const int pair = group * p.group_pairs + in_group % gpairs;
+  const int kvh = pair % p.kv_heads;
+  const int s = pair / p.kv_heads;
   auto active = [&](int t) { return half < 0 || t == half; };
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -749,6 +756,12 @@ int launch_prefill_tc_cfg(const PrefillParams& p, int num_seqs, const CUtensorMa
   PrefillParams q = p;
   q.q_tiles = (p.max_queries + Cfg::kQueries - 1) / Cfg::kQueries;
   q.num_seqs = num_seqs;
+  // Pairs per group: about 48 MB of K/V pages (a third of L2) at the
+  // longest possible sequence.
+  const int64_t pair_bytes =
+      (int64_t)p.max_blocks * BS * D * (KV8 ? 1 : (int64_t)sizeof(T)) * 2;
+  const int64_t pairs_all = (int64_t)p.kv_heads * num_seqs;
+  q.group_pairs = (int)std::max<int64_t>(1, std::min<int64_t>(pairs_all, (48ll << 20) / std::max<int64_t>(pair_bytes, 1)));
   const int64_t items = (int64_t)q.q_tiles * p.kv_heads * num_seqs;
   const int64_t rem = items % sms;
   const int64_t split = (rem > 0 && 2 * rem <= sms) ? rem : 0;
