@@ -10,8 +10,9 @@
 // through the block table.
 //
 // Work decomposition (this library's design): one work item per (query
-// tile, KV head, sequence), on a 1-D grid with the heaviest query tiles
-// first.  An item holds two Q tiles, A and B, of 128 rows each; a row is a
+// tile, KV head, sequence), on a 1-D grid: (KV head, sequence) pairs in
+// groups whose K/V pages fit in a third of L2, the heaviest query tiles
+// first within a group.  An item holds two Q tiles, A and B, of 128 rows each; a row is a
 // (query, grouped head) pair, so the G query heads sharing a KV head share
 // every K/V tile.  One CTA runs an item, except that when the last wave of
 // CTAs would leave at least half the SMs idle, its items run as two CTAs of
