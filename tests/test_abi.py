@@ -91,6 +91,7 @@ def test_decode_argument_errors(lib):
     assert decode(lib, fake_cache(block_size=128)) == -2
     assert decode(lib, c, part=24) == -3                   # not a multiple of b
     assert decode(lib, c, part=16384) == -3
+    assert decode(lib, c, part=8192 + 16) == -3           # just past the largest partition
     assert decode(lib, c, max_len=8 * 16 + 1) == -3        # beyond the table
     assert decode(lib, c, scale=float("nan")) == -3
     assert decode(lib, c, q=0x30002) == -4

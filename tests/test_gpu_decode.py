@@ -130,6 +130,38 @@ def test_partition_boundaries(part, kernel):
     assert np.max(np.abs(gpu_out_f64(out) - ref)) <= TOL["bf16"]
 
 
+@pytest.mark.parametrize("dt,G,b", [("f16", 1, 8), ("bf16", 4, 16), ("f32", 2, 32)])
+def test_largest_partition(dt, G, b, kernel):
+    # Partitions of 8192 positions, the largest accepted: one CTA stages
+    # 8192 / b table entries and streams the whole partition; lengths just
+    # below, at and past it give one full partition, a full one merged with
+    # a one-position one, and a ragged second partition.
+    lens = [1, 8191, 8192, 8193, 9000]
+    c = Case(dt, 2 * G, 2, 128, b, lens, seed=11 + G)
+    out, err = c.gpu(part=8192)
+    assert err == 0
+    ref, bad = c.oracle()
+    assert bad == []
+    assert np.all(np.abs(gpu_out_f64(out) - ref) <= edge_tol(dt, ref))
+
+
+def test_largest_batch(kernel):
+    # 65535 sequences, the most the launch grid indexes: the first, the last
+    # and a seeded spread of sequences against the oracle.
+    S = 65535
+    rng = np.random.default_rng(17)
+    c = Case("bf16", 2, 1, 64, 16, rng.integers(1, 49, S), seed=17, spare=1, width_extra=0)
+    out, err = c.gpu()
+    assert err == 0
+    seqs = sorted({0, 1, S - 2, S - 1, *rng.choice(S, 200, replace=False).tolist()})
+    ref, bad = A.attention(synth.storage_numpy(c.q, "bf16"), synth.storage_numpy(c.k, "bf16"),
+                           synth.storage_numpy(c.v, "bf16"), c.tables, c.lens, c.scale, 16,
+                           "bf16", seqs=seqs)
+    assert bad == []
+    got = gpu_out_f64(out)[seqs]
+    assert np.all(np.abs(got - ref[seqs]) <= edge_tol("bf16", ref[seqs]))
+
+
 def test_invalid_lengths_zero_rows():
     c = Case("f16", 4, 4, 128, 16, [40, 40, 40, 40], seed=6)
     lens = [40, 0, 40, c.width * 16 + 1]

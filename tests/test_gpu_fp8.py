@@ -93,6 +93,16 @@ def test_fp8_decode_matches_oracle(io, G, b, d, part, kernel):
     assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
 
 
+@pytest.mark.parametrize("io,G,b,d", [("bf16", 4, 16, 128), ("f16", 2, 8, 64)])
+def test_fp8_largest_partition(io, G, b, d, kernel):
+    # 8192-position partitions (the largest accepted) over FP8 pools: lengths
+    # below, at and past one partition.
+    lens = [1, 8191, 8192, 8193, 9000]
+    got, ref = decode_case(io, G, b, d, lens, 8192, seed=31 + G)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
+
+
 def test_fp8_step_through_block_manager(kernel):
     # Decode step on an FP8 pool: the block manager plans the step, the new
     # token is quantized into its slot, then attention reads it back.

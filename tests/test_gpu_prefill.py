@@ -146,6 +146,18 @@ def test_prefill_chunked_flow_through_block_manager():
     assert np.max(np.abs(gpu_out_f64(out) - ref)) <= TOL[dt]
 
 
+def test_prefill_sequences_without_queries():
+    # Sequences that bring no queries this step (an empty chunk after a
+    # cached prefix) take no work, raise no error and leave the other
+    # sequences' rows as the oracle gives them.
+    c = PCase("bf16", 8, 2, 128, 16, [40, 100, 0, 77], [5, 0, 130, 0], seed=29)
+    out, err = c.gpu()
+    assert err == 0
+    got, ref = gpu_out_f64(out), c.oracle()
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= edge_tol("bf16", ref))
+
+
 def test_one_query_chunks_agree_with_decode():
     c = PCase("bf16", 32, 8, 128, 16, [10, 500, 77, 1023], [1, 1, 1, 1], seed=4)
     out, err = c.gpu()
