@@ -68,7 +68,8 @@ typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dt
 #define PKV_ERR_WORKSPACE  -5  /* workspace missing or too small                  */
 #define PKV_ERR_CUDA       -6  /* a CUDA runtime call or launch failed            */
 #define PKV_ERR_STATE      -7  /* block manager: unknown / duplicate sequence     */
-#define PKV_ERR_NOMEM      -8  /* block manager: not enough free blocks           */
+#define PKV_ERR_NOMEM      -8  /* block manager: not enough free blocks, or host  */
+                                   /* memory for its bookkeeping ran out              */
 #define PKV_ERR_CAPACITY   -9  /* output table narrower than a sequence's table   */
 
 /* Device error bits (paged_get_device_error). */
@@ -351,7 +352,9 @@ const char* paged_strerror(int code);
  * that reach zero to the free list.  Free-list policy (left open by the
  * pages): blocks are taken from the front of the list, the initial list is
  * `free_order` (NULL = 0..N-1), and freed blocks go back to the front.
- * Not thread-safe; sequences are named by caller-chosen int64 ids.
+ * Not thread-safe; sequences are named by caller-chosen int64 ids.  Every
+ * call is all or nothing: one that fails (including for lack of host memory,
+ * PKV_ERR_NOMEM) leaves the manager unchanged.
  * ------------------------------------------------------------------- */
 typedef struct pkv_block_manager pkv_block_manager;
 

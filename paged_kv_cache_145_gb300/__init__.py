@@ -277,7 +277,8 @@ class BlockManager:
     def admit(self, seq, num_tokens):
         rc = self._lib.pkv_bm_admit(self._h, seq, num_tokens)
         if rc == PKV_ERR_NOMEM:
-            raise MemoryError("not enough free blocks to admit %d positions" % num_tokens)
+            raise MemoryError("not enough free blocks (or host memory) to admit %d positions"
+                              % num_tokens)
         _lib.check(rc, "admit")
 
     def fork(self, parent, child):
@@ -293,7 +294,7 @@ class BlockManager:
         rc = self._lib.pkv_bm_append(self._h, s.ctypes.data, n, slots.ctypes.data,
                                      pairs.ctypes.data, ctypes.byref(npairs))
         if rc == PKV_ERR_NOMEM:
-            raise MemoryError("not enough free blocks for this step")
+            raise MemoryError("not enough free blocks (or host memory) for this step")
         _lib.check(rc, "append")
         return slots, pairs[: npairs.value].copy()
 

@@ -479,7 +479,7 @@ const char* paged_strerror(int code) {
     case PKV_ERR_WORKSPACE: return "workspace missing or too small";
     case PKV_ERR_CUDA: return "CUDA runtime call or kernel launch failed";
     case PKV_ERR_STATE: return "unknown or duplicate sequence id";
-    case PKV_ERR_NOMEM: return "not enough free blocks";
+    case PKV_ERR_NOMEM: return "not enough free blocks (or host memory)";
     case PKV_ERR_CAPACITY: return "table wider than the output capacity";
   }
   return "unknown error code";

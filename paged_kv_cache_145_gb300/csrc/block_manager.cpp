@@ -9,8 +9,11 @@
 // how many positions each block holds, not token contents: the contents live
 // in the device pool.  The free-list policy is documented in
 // include/pagedkv.h (take from the front, return to the front).
+//
+// No C++ exception crosses the C ABI: every call that allocates host memory
+// does so before it changes any state and returns PKV_ERR_NOMEM if an
+// allocation fails, so a failed call leaves the manager as it was.
 #include <cstdint>
-#include <deque>
 #include <new>
 #include <unordered_map>
 #include <vector>
@@ -22,7 +25,10 @@ struct pkv_block_manager {
   int32_t width = 0;
   std::vector<int32_t> refs;  // tables naming each block
   std::vector<int32_t> fill;  // positions stored in each block
-  std::deque<int32_t> free_list;
+  // The free list as a stack: its back is the front of the list.  Capacity
+  // for every block is reserved at creation, so returning a block never
+  // allocates.
+  std::vector<int32_t> free_list;
   struct Seq {
     std::vector<int32_t> table;
     int64_t len = 0;
@@ -30,8 +36,8 @@ struct pkv_block_manager {
   std::unordered_map<int64_t, Seq> seqs;
 
   int32_t take() {
-    const int32_t b = free_list.front();
-    free_list.pop_front();
+    const int32_t b = free_list.back();
+    free_list.pop_back();
     refs[b] = 1;
     fill[b] = 0;
     return b;
@@ -39,10 +45,42 @@ struct pkv_block_manager {
   void unref(int32_t b) {
     if (--refs[b] == 0) {
       fill[b] = 0;
-      free_list.push_front(b);
+      free_list.push_back(b);
     }
   }
 };
+
+namespace {
+
+// The pool invariants that pkv_bm_check reports on (may allocate).
+int check_invariants(const pkv_block_manager& m) {
+  const pkv_block_manager* bm = &m;
+  std::vector<int32_t> count((size_t)bm->num_blocks, 0);
+  for (const auto& kv : bm->seqs) {
+    const auto& t = kv.second.table;
+    if (t.empty()) return PKV_ERR_STATE;
+    int64_t held = 0;
+    for (size_t j = 0; j < t.size(); ++j) {
+      ++count[(size_t)t[j]];
+      const int32_t f = bm->fill[(size_t)t[j]];
+      if (j + 1 < t.size() ? f != bm->width : (f < 1 || f > bm->width)) return PKV_ERR_STATE;
+      held += f;
+    }
+    if (held != kv.second.len) return PKV_ERR_STATE;
+  }
+  std::vector<char> in_free((size_t)bm->num_blocks, 0);
+  for (int32_t b : bm->free_list) {
+    if (in_free[(size_t)b]) return PKV_ERR_STATE;
+    in_free[(size_t)b] = 1;
+  }
+  for (int64_t b = 0; b < bm->num_blocks; ++b) {
+    if (bm->refs[(size_t)b] != count[(size_t)b]) return PKV_ERR_STATE;
+    if ((bm->refs[(size_t)b] == 0) != (in_free[(size_t)b] != 0)) return PKV_ERR_STATE;
+  }
+  return PKV_OK;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -56,6 +94,7 @@ pkv_block_manager* pkv_bm_create(int64_t num_blocks, int32_t block_size,
     bm->width = block_size;
     bm->refs.assign((size_t)num_blocks, 0);
     bm->fill.assign((size_t)num_blocks, 0);
+    bm->free_list.reserve((size_t)num_blocks);
     if (free_order) {
       std::vector<char> seen((size_t)num_blocks, 0);
       for (int64_t i = 0; i < num_blocks; ++i) {
@@ -65,10 +104,10 @@ pkv_block_manager* pkv_bm_create(int64_t num_blocks, int32_t block_size,
           return nullptr;
         }
         seen[(size_t)b] = 1;
-        bm->free_list.push_back((int32_t)b);
       }
+      for (int64_t i = num_blocks - 1; i >= 0; --i) bm->free_list.push_back((int32_t)free_order[i]);
     } else {
-      for (int64_t i = 0; i < num_blocks; ++i) bm->free_list.push_back((int32_t)i);
+      for (int64_t i = num_blocks - 1; i >= 0; --i) bm->free_list.push_back((int32_t)i);
     }
   } catch (...) {
     delete bm;
@@ -83,17 +122,22 @@ int pkv_bm_admit(pkv_block_manager* bm, int64_t seq, int64_t num_tokens) {
   if (!bm) return PKV_ERR_NULL;
   if (num_tokens < 1) return PKV_ERR_ARG;
   if (bm->seqs.count(seq)) return PKV_ERR_STATE;
-  const int64_t need = (num_tokens + bm->width - 1) / bm->width;
+  const int64_t need = num_tokens / bm->width + (num_tokens % bm->width != 0);
   if (need > (int64_t)bm->free_list.size()) return PKV_ERR_NOMEM;
-  pkv_block_manager::Seq s;
-  s.len = num_tokens;
-  s.table.reserve((size_t)need);
+  pkv_block_manager::Seq* s = nullptr;
+  try {  // the only allocations, before any block is taken
+    pkv_block_manager::Seq fresh;
+    fresh.table.reserve((size_t)need);
+    s = &bm->seqs.emplace(seq, std::move(fresh)).first->second;
+  } catch (...) {
+    return PKV_ERR_NOMEM;
+  }
+  s->len = num_tokens;
   for (int64_t i = 0; i < need; ++i) {
     const int32_t b = bm->take();
     bm->fill[b] = (int32_t)(i + 1 < need ? bm->width : num_tokens - (need - 1) * bm->width);
-    s.table.push_back(b);
+    s->table.push_back(b);  // within the reserved capacity
   }
-  bm->seqs.emplace(seq, std::move(s));
   return PKV_OK;
 }
 
@@ -101,9 +145,14 @@ int pkv_bm_fork(pkv_block_manager* bm, int64_t parent, int64_t child) {
   if (!bm) return PKV_ERR_NULL;
   auto it = bm->seqs.find(parent);
   if (it == bm->seqs.end() || bm->seqs.count(child)) return PKV_ERR_STATE;
-  pkv_block_manager::Seq copy = it->second;
-  for (int32_t b : copy.table) ++bm->refs[b];
-  bm->seqs.emplace(child, std::move(copy));
+  const std::vector<int32_t>* table = nullptr;
+  try {
+    pkv_block_manager::Seq copy = it->second;
+    table = &bm->seqs.emplace(child, std::move(copy)).first->second.table;
+  } catch (...) {
+    return PKV_ERR_NOMEM;
+  }
+  for (int32_t b : *table) ++bm->refs[b];
   return PKV_OK;
 }
 
@@ -116,44 +165,55 @@ int pkv_bm_append(pkv_block_manager* bm, const int64_t* seqs, int64_t n, int64_t
   // Dry run: count the fresh blocks the whole step needs, following the
   // same decisions as the real pass (earlier appends in the step can lower a
   // shared block's count or fill a fresh block).  Fresh blocks get negative
-  // stand-in ids.
+  // stand-in ids.  Then reserve table room for every append, so that the
+  // real pass allocates nothing and cannot fail halfway.
   struct Tail {
     int32_t block;
     int32_t fill;
   };
-  std::unordered_map<int64_t, Tail> tails;
-  std::unordered_map<int32_t, int32_t> vrefs;
   int64_t need = 0;
-  for (int64_t i = 0; i < n; ++i) {
-    auto it = bm->seqs.find(seqs[i]);
-    if (it == bm->seqs.end()) return PKV_ERR_STATE;
-    auto tt = tails.find(seqs[i]);
-    Tail t = tt != tails.end() ? tt->second
-                               : Tail{it->second.table.back(), bm->fill[it->second.table.back()]};
-    int32_t r = 1;
-    if (t.block >= 0) {
-      auto rv = vrefs.find(t.block);
-      r = rv != vrefs.end() ? rv->second : bm->refs[t.block];
+  try {
+    std::unordered_map<int64_t, Tail> tails;
+    std::unordered_map<int32_t, int32_t> vrefs;
+    std::unordered_map<int64_t, int64_t> appends;
+    for (int64_t i = 0; i < n; ++i) {
+      auto it = bm->seqs.find(seqs[i]);
+      if (it == bm->seqs.end()) return PKV_ERR_STATE;
+      auto tt = tails.find(seqs[i]);
+      Tail t = tt != tails.end() ? tt->second
+                                 : Tail{it->second.table.back(), bm->fill[it->second.table.back()]};
+      int32_t r = 1;
+      if (t.block >= 0) {
+        auto rv = vrefs.find(t.block);
+        r = rv != vrefs.end() ? rv->second : bm->refs[t.block];
+      }
+      if (t.fill == bm->width) {
+        ++need;
+        t = Tail{(int32_t)-need, 1};
+      } else if (r > 1) {
+        vrefs[t.block] = r - 1;
+        ++need;
+        t = Tail{(int32_t)-need, t.fill + 1};
+      } else {
+        ++t.fill;
+      }
+      tails[seqs[i]] = t;
+      ++appends[seqs[i]];
     }
-    if (t.fill == bm->width) {
-      ++need;
-      t = Tail{(int32_t)-need, 1};
-    } else if (r > 1) {
-      vrefs[t.block] = r - 1;
-      ++need;
-      t = Tail{(int32_t)-need, t.fill + 1};
-    } else {
-      ++t.fill;
+    if (need > (int64_t)bm->free_list.size()) return PKV_ERR_NOMEM;
+    for (const auto& kv : appends) {
+      auto& table = bm->seqs.find(kv.first)->second.table;
+      table.reserve(table.size() + (size_t)kv.second);
     }
-    tails[seqs[i]] = t;
+  } catch (...) {
+    return PKV_ERR_NOMEM;
   }
-  if (need > (int64_t)bm->free_list.size()) return PKV_ERR_NOMEM;
   int64_t np = 0;
   for (int64_t i = 0; i < n; ++i) {
-    auto& s = bm->seqs[seqs[i]];
+    auto& s = bm->seqs.find(seqs[i])->second;
     const int32_t last = s.table.back();
     if (bm->fill[last] == bm->width) {
-      s.table.push_back(bm->take());
+      s.table.push_back(bm->take());  // within the reserved capacity
     } else if (bm->refs[last] > 1) {
       const int32_t fresh = bm->take();
       bm->fill[fresh] = bm->fill[last];
@@ -207,7 +267,8 @@ int pkv_bm_slots(const pkv_block_manager* bm, int64_t seq, int64_t start, int64_
   if (!bm) return PKV_ERR_NULL;
   auto it = bm->seqs.find(seq);
   if (it == bm->seqs.end()) return PKV_ERR_STATE;
-  if (start < 0 || count < 0 || start + count > it->second.len) return PKV_ERR_ARG;
+  if (start < 0 || count < 0 || start > it->second.len || count > it->second.len - start)
+    return PKV_ERR_ARG;
   if (count > 0 && !slot_mapping) return PKV_ERR_NULL;
   const auto& table = it->second.table;
   for (int64_t i = 0; i < count; ++i) {
@@ -240,29 +301,11 @@ int32_t pkv_bm_refcount(const pkv_block_manager* bm, int64_t block) {
 
 int pkv_bm_check(const pkv_block_manager* bm) {
   if (!bm) return PKV_ERR_NULL;
-  std::vector<int32_t> count((size_t)bm->num_blocks, 0);
-  for (const auto& kv : bm->seqs) {
-    const auto& t = kv.second.table;
-    if (t.empty()) return PKV_ERR_STATE;
-    int64_t held = 0;
-    for (size_t j = 0; j < t.size(); ++j) {
-      ++count[(size_t)t[j]];
-      const int32_t f = bm->fill[(size_t)t[j]];
-      if (j + 1 < t.size() ? f != bm->width : (f < 1 || f > bm->width)) return PKV_ERR_STATE;
-      held += f;
-    }
-    if (held != kv.second.len) return PKV_ERR_STATE;
+  try {
+    return check_invariants(*bm);
+  } catch (...) {
+    return PKV_ERR_NOMEM;
   }
-  std::vector<char> in_free((size_t)bm->num_blocks, 0);
-  for (int32_t b : bm->free_list) {
-    if (in_free[(size_t)b]) return PKV_ERR_STATE;
-    in_free[(size_t)b] = 1;
-  }
-  for (int64_t b = 0; b < bm->num_blocks; ++b) {
-    if (bm->refs[(size_t)b] != count[(size_t)b]) return PKV_ERR_STATE;
-    if ((bm->refs[(size_t)b] == 0) != (in_free[(size_t)b] != 0)) return PKV_ERR_STATE;
-  }
-  return PKV_OK;
 }
 
 }  // extern "C"

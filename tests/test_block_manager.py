@@ -141,6 +141,21 @@ def test_bad_arguments():
         bm.tables([0], 0)
 
 
+def test_oversized_requests_change_nothing():
+    # Requests whose rounded-up block count or position range would overflow
+    # 64 bits are refused, and the manager is left as it was.
+    bm = BlockManager(8, 16)
+    bm.admit(0, 20)
+    free = bm.num_free()
+    for n in (2**62, 2**63 - 1):
+        with pytest.raises(MemoryError):
+            bm.admit(1, n)
+    assert bm.num_free() == free and bm.seq_len(1) == -1 and bm.check()
+    assert bm._lib.pkv_bm_slots(bm._h, 0, 1, 2**63 - 1, None) == -3   # start + count overflows
+    assert list(bm.slots(0, 0, 20)) == [bm.tables([0], 2)[0][0][t // 16] * 16 + t % 16
+                                        for t in range(20)]
+
+
 def test_slots_query_matches_oracle_translation():
     rng = random.Random(9)
     order = rng.sample(range(64), 64)
