@@ -147,17 +147,27 @@ def check_cow_demo(BlockPool):
     small = BlockPool(int(g["small_pool_blocks"]), int(g["block_width"]))
     small.admit("A", ints(g["small_parent_tokens"]))
     small.fork("A", "B")
-    before = (small.read("A"), small.read("B"), list(small.refcount))
+    before = (small.read("A"), small.read("B"), small.refcounts(), list(small.slots))
     failed = False
     try:
         small.append("B", int(g["small_child_token"]))
     except MemoryError:
         failed = True
     assert failed
-    assert before == (small.read("A"), small.read("B"), list(small.refcount))
-    # Negative control: mutating the shared tail directly corrupts A.
-    small.payload[small.table("B")[-1]].append(int(g["negative_control_token"]))
-    assert small.read("A") == ints(g["negative_control_parent_after"])
+    assert before == (small.read("A"), small.read("B"), small.refcounts(), list(small.slots))
+    # Negative control: B's next token written straight into the shared tail
+    # (no copy) lands in the block A reads through, which then holds 1, 2, 99,
+    # and the recomputed invariants flag the block as shared with two fills.
+    t, w = small.length("B"), small.width
+    small.slots[small.table("B")[t // w] * w + t % w] = int(g["negative_control_token"])
+    small.lengths["B"] = t + 1
+    assert small.block_contents(small.table("A")[-1]) == ints(g["negative_control_parent_after"])
+    try:
+        small.verify()
+        caught = False
+    except AssertionError:
+        caught = True
+    assert caught
 
 
 def check_fork_workload(BlockPool, b=16, prompt=1031, forks=8):
@@ -182,8 +192,8 @@ def check_fork_workload(BlockPool, b=16, prompt=1031, forks=8):
     for f in range(forks):
         assert pool.table(f)[:full] == shared
         assert pool.read(f) == list(range(prompt)) + [10_000 + f]
-        assert pool.refcount[pool.table(f)[-1]] == 1
-    assert all(pool.refcount[blk] == forks for blk in shared)
+        assert pool.refcounts()[pool.table(f)[-1]] == 1
+    assert all(pool.refcounts()[blk] == forks for blk in shared)
     assert 200 - pool.num_free() == full + forks
     assert len({pool.table(f)[-1] for f in range(forks)}) == forks
 

@@ -22,8 +22,9 @@ def same_state(bm, pool, names):
         assert list(tab[0]) == pool.table(n)
         assert int(lens[0]) == pool.length(n) == bm.seq_len(n)
     assert bm.num_free() == pool.num_free()
+    counts = pool.refcounts()
     for blk in range(pool.num_blocks):
-        assert bm.refcount(blk) == pool.refcount[blk]
+        assert bm.refcount(blk) == counts[blk]
     assert bm.check()
 
 

@@ -97,12 +97,21 @@ def test_merge_without_rescale():
 
 def test_append_without_copy_on_write():
     fails(pins.check_cow_demo,
-          mutant(B.BlockPool, "cow = (not grow) and self.refcount[last] > 1", "cow = False"))
+          mutant(B.BlockPool, "shared = not full and self.holders_of_tail(tail) > 1", "shared = False"))
+
+
+def test_copy_on_write_without_the_copy():
+    fails(pins.check_cow_demo, mutant(B.BlockPool, "self._duplicate(tail, mine)", "pass"))
+
+
+def test_tail_fill_off_by_one_block():
+    bad = mutant(B.BlockPool, "(len(self.tables[name]) - 1) * self.width",
+                 "len(self.tables[name]) * self.width")
+    fails(pins.check_pool_vs_contiguous, bad, P.allocated_slots)
 
 
 def test_release_ignores_sharing():
-    bad = mutant(B.BlockPool, "self.refcount[blk] -= 1\n        if self.refcount[blk] == 0:",
-                 "self.refcount[blk] = 0\n        if True:")
+    bad = mutant(B.BlockPool, "if blk not in still_held:", "if True:")
     fails(pins.check_pool_vs_contiguous, bad, P.allocated_slots)
 
 
