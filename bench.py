@@ -9,9 +9,11 @@ pass and, when a sequence spans several partitions, the split-K merge); on
 the parallel-sampling workload the copy-on-write block copies run first.
 The default workload is the OPT-13B-shaped decode (40 heads MHA, head_dim
 128, fp16, block 16, batch 64, lengths uniform over 200..2000, shuffled pool
-= need + 10%), one layer.  Inputs are seeded synthetic data resident in HBM;
-the pool (about 1.6 GB) is larger than L2, so no flush is needed between
-steps.
+= need + 10%), one layer.  The default line also carries, under the key
+"gqa", the same measurement of the GQA Llama-3-8B-shaped decode (32 query /
+8 KV heads, bf16, batch 256).  Inputs are seeded synthetic data resident in
+HBM; the pools (about 1.6 and 1.3 GB) are larger than L2, so no flush is
+needed between steps.
 
 The timed region runs K steps back to back (device time between one event
 before the first and one after the last) and then K decode launches alone,
@@ -207,6 +209,38 @@ def e2e_graphed(host_tensors, dev, step, out_like, steps, per_graph=8):
     last = (per_graph - 1) % 2
     return (start.elapsed_time(end) / 1e3 / n, staged[0][0].numel(),
             outs_h[0].numel() * outs_h[0].element_size(), outs_h[last], outs[last]), n
+
+
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
+
+
+def read_stream_gbs(dev, nbytes=4 << 30, reps=10):
+    """A measured read-only streaming rate: the library's read-stream
+    self-test kernel over a buffer far larger than L2, best of ``reps``
+    CUDA-event timed passes.  Context for the roofline, next to the
+    copy-rate peak."""
+    import torch
+
+    import paged_kv_cache_145_gb300 as pkv
+
+    x = torch.ones(nbytes, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        pkv.paged_selftest_read_stream(x, sink)
+    best = None
+    stream = torch.cuda.current_stream()
+    for _ in range(reps):
+        a, z = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        pkv.paged_selftest_read_stream(x, sink)
+        z.record(stream)
+        z.synchronize()
+        t = a.elapsed_time(z) / 1e3
+        best = t if best is None else min(best, t)
+    del x
+    return {"gbs": round(nbytes / best / 1e9, 1),
+            "how": "paged_selftest_read_stream (16-byte non-caching loads, whole GPU) over "
+                   "%d MiB, best of %d" % (nbytes >> 20, reps)}
 
 
 def hbm_peak():
@@ -505,6 +539,78 @@ def oracle_timed(name, budget_s, seed=4242):
     return oracle_child(_oracle_sample, name, budget_s, seed)
 
 
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def _oracle_worker(name, budget_s, seed, w, workers, start, results):
+    """One of ``workers`` oracle processes: sequences w, w + workers, ... of
+    the workload (cycling), prepared before the common start, then timed
+    until ``budget_s`` seconds of oracle work have passed."""
+    lengths = _lengths(name)
+    mine = list(range(w, len(lengths), workers)) or [w % len(lengths)]
+    prepared = {}
+
+    def get(i):
+        if i not in prepared:
+            prepared[i] = _oracle_prepare(name, i, int(lengths[i]), seed)
+        return prepared[i]
+
+    get(mine[0])
+    start.wait()
+    kv_bytes, done, spent, k = 0, 0, 0.0, 0
+    while spent < budget_s:
+        x = get(mine[k % len(mine)])
+        spent += _oracle_step(x)
+        kv_bytes += x["kv_bytes"]
+        done += 1
+        k += 1
+    results.put((kv_bytes, spent, done))
+
+
+def oracle_all_cores(name, budget_s, seed=4242):
+    """The oracle spread over every host core the process may use: one
+    spawned process per core (one BLAS thread each), each on its own share
+    of the workload's sequences, started together.  Returns (kv_bytes,
+    seconds, seqs, workers); throughput = all bytes over the longest
+    worker's time."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    workers = host_cores()
+    ctx = mp.get_context("spawn")
+    start, results = ctx.Barrier(workers), ctx.Queue()
+    procs = [ctx.Process(target=_oracle_worker,
+                         args=(name, budget_s, seed, w, workers, start, results))
+             for w in range(workers)]
+    for p in procs:
+        p.start()
+    got = [results.get() for _ in procs]
+    for p in procs:
+        p.join()
+    return (sum(g[0] for g in got), max(g[1] for g in got), sum(g[2] for g in got), workers)
+
+
+def cpu_baseline_record(name, single, pool, num_seqs, what):
+    """cpu_baseline: the one-process oracle figure, with the all-cores one
+    beside it."""
+    cb, cs, cn = single
+    rec = {"value": round(cb / cs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+           "sample": "%d of %d sequences (all heads), %s, float64 NumPy oracle, 1 process, "
+                     "1 BLAS thread, %.1f s" % (cn, num_seqs, what, cs),
+           "host_cores": host_cores(), "blas_threads": 1}
+    if pool is not None:
+        pb, ps, pn, pw = pool
+        rec["all_cores"] = {
+            "value": round(pb / ps / 1e9, 6), "unit": "GB/s", "cores": pw, "kind": "oracle",
+            "sample": "%d processes (one per host core, 1 BLAS thread each) over strided "
+                      "shares of the %d sequences, cycling, %d sequence steps in %.1f s; "
+                      "all bytes over the longest process's time" % (pw, num_seqs, pn, ps)}
+    return rec
+
+
 def _oracle_prefill_sample(name, budget_s, seed, fp8):
     """Times the oracle's chunk write + causal prefill attention over the
     workload's sequences, one (sequence, KV head) pair at a time with that
@@ -636,6 +742,7 @@ def run_reference(args):
         # a step over h of the KV heads counts as h / kv_heads of a sequence
         "decode_tokens_per_s": round(seqs * h / hk / total_s, 3),
         "cpu_baseline": {"value": round(gbs, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "host_cores": host_cores(), "blas_threads": 1,
                          "sample": "%d steps of one sequence each (8 distinct, cycled; "
                                    "%d of %d KV heads), float64 NumPy oracle (write + "
                                    "attention), 1 BLAS thread" % (seqs, h, hk)},
@@ -658,16 +765,51 @@ def run_ours(args):
     dev = torch.device("cuda", local_rank)
     pkv._lib.lib()
 
-    # The CPU baseline child is spawned before any GPU work.
-    cpu = None
+    # The default line also measures the GQA workload (32 query / 8 KV heads,
+    # bf16, batch 256), under the key "gqa", with its own roofline, clocks,
+    # end-to-end figure and CPU baseline; the headline stays the
+    # OPT-13B-shaped workload.
+    names = [args.config]
+    if (args.config == "opt13b" and args.kv_dtype == "native" and args.partition == 0
+            and args.block_size == 0 and args.table == "shuffled" and not args.no_gqa):
+        names.append("gqa")
+
+    # The CPU baselines run before any GPU work, so the oracle processes do
+    # not compete with the timed region for host cores.
+    cpu = {}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = oracle_timed(args.config, args.cpu_budget)
+        for name in names:
+            single = oracle_timed(name, args.cpu_budget)
+            pool = oracle_all_cores(name, args.cpu_budget / 2) if not args.no_all_cores else None
+            cpu[name] = (single, pool)
+
+    line = decode_line(args, args.config, cpu.get(args.config), rank, local_rank, world, dev)
+    for name in names[1:]:
+        torch.cuda.empty_cache()
+        sub = decode_line(args, name, cpu.get(name), rank, local_rank, world, dev)
+        if rank == 0:
+            line[name] = {k: sub[k] for k in SUB_RECORD_KEYS if k in sub}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+SUB_RECORD_KEYS = ("metric", "value", "unit", "steps", "warmup", "ms_per_step", "dtype", "config",
+                   "decode_tokens_per_s", "kv_gbs", "layer_stack_extrapolation", "roofline",
+                   "clocks", "gpu_launches", "e2e", "e2e_eager", "cpu_baseline")
+
+
+def decode_line(args, name, cpu, rank, local_rank, world, dev):
+    """Times the decode step of workload ``name`` and returns its JSON line
+    (rank 0) or None (other ranks)."""
+    import torch
+
+    import paged_kv_cache_145_gb300 as pkv
 
     kv_dtype = "e4m3" if args.kv_dtype == "fp8" else None
-    w = Workload(args.config, rank=rank, block_size=args.block_size or None, table=args.table,
+    w = Workload(name, rank=rank, block_size=args.block_size or None, table=args.table,
                  kv_dtype=kv_dtype)
     dt = synth.TORCH_DTYPE[w.dtype]
-    seed = synth.seed_of(args.config, 3) + 10 * rank
+    seed = synth.seed_of(name, 3) + 10 * rank
     shape = (w.N, w.Hk, w.b, w.D)
     if kv_dtype:
         # FP8 E4M3 pool with one scale per KV head (1/64: N(0, 1) values
@@ -823,8 +965,9 @@ def run_ours(args):
     eager_bytes, eager_max_s = combine_ranks(step_bytes, eager_s or 0.0)  # every rank calls it
     all_seqs, _ = combine_ranks(w.S * args.steps, total_ms / 1e3)
     if rank != 0:
-        return
+        return None
     peak, peak_kind = hbm_peak()
+    read_peak = read_stream_gbs(dev)
     unique_bytes = w.unique_kv_bytes()
     # Pages shared by several tables (forks) are fetched from DRAM once and
     # then served from L2: the roofline counts them once.
@@ -833,7 +976,7 @@ def run_ours(args):
     layers = w.cfg.get("layers", 1)
     src_hash = kernel_source_hash("fp8" if kv_dtype else "native")
     default_shape = args.partition == 0 and args.block_size == 0 and args.table == "shuffled"
-    key = "%s/%s/%d" % (args.config, "fp8" if kv_dtype else "native", part)
+    key = "%s/%s/%d" % (name, "fp8" if kv_dtype else "native", part)
     tr = TRAFFIC.get(key) if default_shape else None
     traffic = tr[0] if tr and tr[1] == src_hash else None
     line = {
@@ -849,7 +992,7 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": w.dtype if not kv_dtype else "%s (KV cache e4m3)" % w.dtype,
         "data": "synthetic",
-        "config": {"workload": args.config, "about": w.cfg["about"], "num_seqs": w.S,
+        "config": {"workload": name, "about": w.cfg["about"], "num_seqs": w.S,
                    "kv_dtype": w.kv_dtype,
                    "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
                    "pool_blocks": w.N, "partition_size": part, "table": w.table_kind,
@@ -871,7 +1014,13 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "paged_attention_decode (partition pass + split-K merge)",
-                     "peak_source": peak_kind, "decode_us": round(decode_ms * 1e3, 2),
+                     "peak_source": peak_kind,
+                     "peak_note": ("the measured device-to-device copy rate (half reads, half "
+                                   "writes); decode only reads, so it can exceed 1.0"),
+                     "nominal_peak": NOMINAL_HBM_GBS,
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "read_stream": read_peak,
+                     "decode_us": round(decode_ms * 1e3, 2),
                      "decode_bytes": roof_bytes, "source_hash": src_hash,
                      "basis": ("distinct positions (shared pages counted once)"
                                if unique_bytes < kv_bytes else "every position read")},
@@ -879,14 +1028,17 @@ def run_ours(args):
         "gpu_launches": (launches_per_step + decode_launches) * args.steps,
         "e2e": {"value": round(all_e2e_bytes / max_e2e_s / 1e9, 3), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5), "copies": e2e_mode},
+                "ms_per_step": round(max_e2e_s * 1e3 / e2e_steps, 5), "copies": e2e_mode,
+                "mode": "graph replay" if eager_s is not None else "eager (one API call per step)"},
     }
     if eager_s is not None:
         line["e2e_eager"] = {
             "value": round(eager_bytes / eager_max_s / 1e9, 3), "unit": "GB/s",
             "ms_per_step": round(eager_max_s * 1e3, 5),
-            "note": "the same pipelined steps issued one at a time from Python; bound by the "
-                    "host's per-step launch work when that exceeds the step's device time"}
+            "mode": "eager (one API call per step)",
+            "note": "the per-call API figure: the same pipelined steps issued one at a time "
+                    "from Python through the binding and the C ABI; bound by the host's "
+                    "per-step launch work when that exceeds the step's device time"}
     if warm is not None:
         line["warm_l2"] = {
             "ms_per_step": round(warm[0] / args.steps, 5),
@@ -895,12 +1047,9 @@ def run_ours(args):
             "kv_unique_gbs": round(unique_bytes / (warm[1] / 1e3) / 1e9, 3),
             "note": "same steps back to back with no flush: shared and small pools hit L2"}
     if cpu is not None:
-        cb, cs, cn = cpu
-        line["cpu_baseline"] = {
-            "value": round(cb / cs / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d sequences (all heads), KV write + attention, float64 NumPy "
-                      "oracle, 1 BLAS thread, %.1f s" % (cn, w.S, cs)}
-    print(json.dumps(line), flush=True)
+        line["cpu_baseline"] = cpu_baseline_record(name, cpu[0], cpu[1], w.S,
+                                                   "KV write + attention")
+    return line
 
 
 # ---------------------------------------------------------------------------
@@ -1211,6 +1360,10 @@ def main():
                          "chunk write + causal prefill attention (--config prefill|chunked)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-all-cores", action="store_true",
+                    help="skip the all-cores oracle figure beside the one-process one")
+    ap.add_argument("--no-gqa", action="store_true",
+                    help="default line: skip the GQA workload's sub-record")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

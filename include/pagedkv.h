@@ -78,6 +78,10 @@ typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dt
 #define PKV_DEV_SEQ_LEN      4u  /* decode: length not in [1, max_seq_len]        */
 #define PKV_DEV_PAIR_RANGE   8u  /* paged_block_copy: src or dst not in [0, N)    */
 #define PKV_DEV_TIMEOUT     16u  /* a bounded wait for a bulk copy gave up        */
+/* After PKV_DEV_TIMEOUT the launch that set it may have ended with bulk
+ * copies still in flight into its shared memory (the drain after a timeout
+ * is itself bounded).  Treat the stream as failed: that launch's outputs,
+ * and the results of any later launch on the same device, are suspect. */
 
 /* The paged pool.  Supported geometry: block_size in {8, 16, 32, 64},
  * head_dim in {64, 128}.  k_cache / v_cache must be 16-byte aligned. */
@@ -252,8 +256,12 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
  *     report it, exceeds PKV_STATIC_WS_BYTES returns PKV_ERR_WORKSPACE and
  *     enqueues nothing.
  *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current) and caches it; make
- *     that first call before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it.  With
+ *     lazy module loading that lookup is also when the 32 MiB are committed
+ *     on the device, so make the first call before the host program reserves
+ *     its device memory, and before any stream capture.  If the lookup
+ *     fails the call returns PKV_ERR_CUDA and clears the runtime's error, so
+ *     later calls are not affected.
  *   - All calls share the one array.  Calls whose kernels overlap on the GPU
  *     (different streams, no ordering between them) race on it and give
  *     wrong results; order them on one stream or with events.  Each call
@@ -333,6 +341,19 @@ int paged_get_device_error(cudaStream_t stream, uint32_t* bits);
  * the range.
  */
 int paged_selftest_wait_timeout(uint64_t limit_ns, cudaStream_t stream);
+
+/*
+ * paged_selftest_read_stream -- reads every byte of a device buffer once
+ * (16-byte non-caching loads over the whole GPU) and XOR-folds the words
+ * into *sink.  The pages have no counterpart: it measures the read-only
+ * streaming bandwidth that the decode kernels, which only read the pool,
+ * are compared with.
+ *
+ *   buf    device, 16-byte aligned, `bytes` a multiple of 16 (else
+ *          PKV_ERR_ALIGN); 0 bytes launches nothing (buf may be NULL)
+ *   sink   device uint32; XOR-updated (its value has no meaning)
+ */
+int paged_selftest_read_stream(const void* buf, size_t bytes, uint32_t* sink, cudaStream_t stream);
 
 /* Text for a PKV_ERR_* code. */
 const char* paged_strerror(int code);

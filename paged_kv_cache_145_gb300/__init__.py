@@ -29,7 +29,7 @@ __all__ = [
     "paged_attention_prefill",
     "paged_attention_workspace_bytes", "paged_attention_partition_size",
     "paged_block_copy", "paged_block_swap", "paged_get_device_error",
-    "paged_selftest_wait_timeout", "library_path",
+    "paged_selftest_wait_timeout", "paged_selftest_read_stream", "library_path",
 ]
 
 
@@ -246,6 +246,18 @@ def paged_selftest_wait_timeout(limit_ns=10_000_000, stream=None):
     :func:`paged_get_device_error`)."""
     _lib.check(_lib.lib().paged_selftest_wait_timeout(int(limit_ns), _stream(stream)),
                "paged_selftest_wait_timeout")
+
+
+def paged_selftest_read_stream(buf, sink, stream=None):
+    """Read every byte of the device tensor ``buf`` once (read-only
+    streaming bandwidth); ``sink`` is a device int32 tensor of one element
+    that the kernel XOR-updates."""
+    if not buf.is_cuda or not buf.is_contiguous():
+        raise ValueError("buf must be a contiguous CUDA tensor")
+    _need(sink, "sink", torch.int32, buf.device)
+    _lib.check(_lib.lib().paged_selftest_read_stream(_ptr(buf), buf.numel() * buf.element_size(),
+                                                     _ptr(sink), _stream(stream)),
+               "paged_selftest_read_stream")
 
 
 def _i64(a):

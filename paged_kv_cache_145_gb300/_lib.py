@@ -59,6 +59,7 @@ SIGNATURES = {
     "paged_block_swap": (ctypes.c_int, [_CACHE, _P, _P, _I64, _P, _I64, _I32, _P]),
     "paged_get_device_error": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "paged_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint64, _P]),
+    "paged_selftest_read_stream": (ctypes.c_int, [_P, ctypes.c_size_t, _P, _P]),
     "paged_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pkv_bm_create": (_P, [_I64, _I32, _P]),
     "pkv_bm_destroy": (None, [_P]),

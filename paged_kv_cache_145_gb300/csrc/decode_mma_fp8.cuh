@@ -12,9 +12,10 @@
 // way in the query fragments, so the dot products are unchanged.  Values
 // are widened into a swizzled 16-bit tile (they must be transposed for
 // P . V, which `ldmatrix` does on 16-bit data).  Both products run in fp16
-// (every E4M3 value is exact in fp16, P keeps 11 bits and needs no high/low
-// split); bf16 queries are converted to fp16, exact for magnitudes in
-// [2^-14, 2^15) and kept in range by a power-of-two scale of the group.
+// (every E4M3 value is exact in fp16; P keeps 11 bits, or about 22 as two
+// fp16 parts for heads whose value scale needs it, see fp8_split_p); bf16
+// queries are converted to fp16, exact for magnitudes in [2^-14, 2^15) and
+// kept in range by a power-of-two scale of the group.
 //
 // decode_partition_mma_fp8_widen_kernel (head_dim 64).  Widens both keys and
 // values into 16-bit tiles and reuses the fp16/bf16 fragment code.
@@ -44,7 +45,7 @@ struct Fp8WidenCfg {
   static constexpr int kRawOff = kWideBytes;
   static constexpr int kBarOff = kRawOff + kWarps * kStages * kRawStage;
   static constexpr int kPtOff = kBarOff + kWarps * kStages * 8;
-  static constexpr int kPtBytes = 8 * kChunk * 2;         // P^T, fp16
+  static constexpr int kPtBytes = 2 * 8 * kChunk * 2;     // P^T, fp16, and its low part
   static constexpr int kTableOff = kPtOff + kWarps * kPtBytes;
   static constexpr int kAlign = 1024;
   static constexpr int kMergeBytes = (kWarps * G * D + 3 * kWarps * G + 2 * G) * 4;
@@ -77,6 +78,37 @@ __device__ __forceinline__ void widen16(const uint4& c, uint4& lo, uint4& hi) {
   }
   lo = make_uint4(out[0], out[1], out[2], out[3]);
   hi = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+// P enters P.V in fp16 (unit roundoff 2^-11) and the values are codes of
+// magnitude up to 448 times the head's value scale, so rounding P moves an
+// output by at most 2^-11 * 448 * |v_scale|.  When that bound could exceed
+// half of the output type's error bar for attention (max abs 2e-3 for fp16
+// outputs, 8e-3 for bf16), P is used as two fp16 parts, the rounded value
+// and the rounded remainder (about 22 significant bits), with one P.V
+// product per part.  The other half of the bar covers the output's own
+// rounding.  T is the output type.
+template <typename T>
+__device__ __forceinline__ bool fp8_split_p(float v_scale) {
+  const float half_bar = std::is_same<T, __half>::value ? 1e-3f : 4e-3f;
+  return 448.f * 0x1p-11f * fabsf(v_scale) > half_bar;
+}
+
+// P^T of one chunk through shared memory: lane (gi, ti) holds P of
+// positions gi and gi + 8 for heads 2ti, 2ti + 1; entry [head][position]
+// (C positions per head) holds its fp16 bits, and, when split, the fp16
+// bits of the remainder 8 * C entries further.
+template <int C>
+__device__ __forceinline__ void stage_pt(uint16_t* pt, int gi, int ti, const float (&pr)[4],
+                                         bool split) {
+  const int idx[4] = {(2 * ti) * C + gi, (2 * ti + 1) * C + gi, (2 * ti) * C + gi + 8,
+                      (2 * ti + 1) * C + gi + 8};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __half h = __float2half_rn(pr[i]);
+    pt[idx[i]] = __half_as_ushort(h);
+    if (split) pt[8 * C + idx[i]] = __half_as_ushort(__float2half_rn(pr[i] - __half2float(h)));
+  }
 }
 
 // Widens the four E4M3 codes of a 32-bit word into two fp16 pairs
@@ -225,6 +257,7 @@ decode_partition_mma_fp8_widen_kernel(const DecodeParams p) {
   unsigned char* vtw = ktw + Cfg::kTileBytes;              // widened values
   const uint32_t ktile = smem_addr(ktw), vtile = smem_addr(vtw);
   uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
+  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);  // the same for the whole CTA
 
   int j = 0;
   for (; j < count; ++j) {
@@ -311,16 +344,15 @@ decode_partition_mma_fp8_widen_kernel(const DecodeParams p) {
     }
 
     // ---- P^T (fp16) through shared memory ---------------------------------
-    pt[(2 * ti) * C + gi] = OpV::bits(pr[0]);
-    pt[(2 * ti + 1) * C + gi] = OpV::bits(pr[1]);
-    pt[(2 * ti) * C + gi + 8] = OpV::bits(pr[2]);
-    pt[(2 * ti + 1) * C + gi + 8] = OpV::bits(pr[3]);
+    stage_pt<C>(pt, gi, ti, pr, split_p);
     __syncwarp();
     const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
     const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
     const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
+    const uint32_t b0l = split_p ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
+    const uint32_t b1l = split_p ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
 
-    // ---- O^T += V^T . P^T (fp16) -------------------------------------------
+    // ---- O^T += V^T . P^T (fp16; low part too when split) -------------------
 #pragma unroll
     for (int i = 0; i < KSTEPS; ++i) {
       const int col8 = 2 * (i % 4) + v_col8;
@@ -329,6 +361,7 @@ decode_partition_mma_fp8_widen_kernel(const DecodeParams p) {
       uint32_t a[4];
       ldsm_x4_trans(a, addr);
       OpV::run(acc[i], a, b0, b1);
+      if (split_p) OpV::run(acc[i], a, b0l, b1l);
     }
     __syncwarp();  // the widened tiles and P^T are rewritten next chunk
   }
@@ -410,7 +443,7 @@ struct Fp8MmaCfg {
   static constexpr int kRingBytes = kWarps * kStages * kRawStage;
   static constexpr int kBarOff = kRingBytes;
   static constexpr int kPtOff = kBarOff + kWarps * kStages * 8;
-  static constexpr int kPtBytes = 8 * kChunk * 2;
+  static constexpr int kPtBytes = 2 * 8 * kChunk * 2;  // P^T, fp16, and its low part
   static constexpr int kTableOff = kPtOff + kWarps * kPtBytes;
   static constexpr int kAlign = 1024;
   static constexpr int kMergeBytes = (kWarps * G * D + 3 * kWarps * G + 2 * G) * 4;
@@ -574,6 +607,7 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
   const int k_row = (mm & 1) * 8 + mr;  // ldmatrix row this lane addresses (keys)
   const int k_half = mm >> 1;           // which 16-code chunk of the pair
   uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
+  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);  // the same for the whole CTA
 
   int j = 0;
   for (; j < count; ++j) {
@@ -636,14 +670,13 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
         acc[i][3] *= alpha[1];
       }
     }
-    pt[(2 * ti) * C + gi] = Op::bits(pr[0]);
-    pt[(2 * ti + 1) * C + gi] = Op::bits(pr[1]);
-    pt[(2 * ti) * C + gi + 8] = Op::bits(pr[2]);
-    pt[(2 * ti + 1) * C + gi + 8] = Op::bits(pr[3]);
+    stage_pt<C>(pt, gi, ti, pr, split_p);
     __syncwarp();
     const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
     const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
     const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
+    const uint32_t b0l = split_p ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
+    const uint32_t b1l = split_p ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
 
     // ---- O^T += V^T . P^T, value fragments straight from the codes --------
     // The contraction runs over positions, which sit in different code rows,
@@ -674,6 +707,10 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
         e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x7362), b[2], b[3]);
         Op::run(acc[2 * q], a, b0, b1);
         Op::run(acc[2 * q + 1], b, b0, b1);
+        if (split_p) {
+          Op::run(acc[2 * q], a, b0l, b1l);
+          Op::run(acc[2 * q + 1], b, b0l, b1l);
+        }
       }
     }
     __syncwarp();  // the raw stage and P^T are rewritten next

@@ -28,11 +28,19 @@ void* g_static_ptr[kMaxDevices] = {};
 // device (on that device's first call) and cached.
 void* static_ws_address() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
   std::lock_guard<std::mutex> lock(g_static_mu);
   if (!g_static_ptr[dev]) {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_pkv_static_ws) != cudaSuccess || !ptr) return nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_pkv_static_ws) != cudaSuccess || !ptr) {
+      // Clear the runtime's last error: the launchers judge their own
+      // launches with cudaPeekAtLastError and must not see this one.
+      (void)cudaGetLastError();
+      return nullptr;
+    }
     g_static_ptr[dev] = ptr;
   }
   return g_static_ptr[dev];

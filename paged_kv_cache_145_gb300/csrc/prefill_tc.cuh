@@ -36,8 +36,9 @@
 //   warps 11-14 (FP8 pools only) converters: widen the producer's raw code
 //              tiles into the fp16 operand tiles (exact), writing zeros for
 //              value rows past the last needed key.  Both products then run
-//              in fp16 with P unsplit; bf16 queries enter as fp16 with a
-//              per-row power-of-two shift.
+//              in fp16; P is split into two fp16 parts only for heads whose
+//              value scale needs it (fp8_split_p); bf16 queries enter as
+//              fp16 with a per-row power-of-two shift.
 // The running maximum is raised lazily: O and the sum are rescaled only
 // when a row's maximum grows by more than 2^8, so P stays at or below 256
 // and most tiles skip the tensor-memory round trip of O.
@@ -358,6 +359,11 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
   tc_fence_after();
   const uint32_t tmem = *slot;
   bool failed = false;
+  // P in two parts (a second P.V MMA): bf16 pools always; FP8 pools when
+  // the head's value scale makes fp16 P too coarse (fp8_split_p, with the
+  // FP8 decode kernels).
+  bool split_p = Cfg::kSplitP;
+  if constexpr (KV8) split_p = fp8_split_p<T>(p.v_scale[kvh]);
 
   if (warp == Cfg::kProducerWarp) {
     // ---- producer: K and V tiles ------------------------------------------
@@ -470,7 +476,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
           // P of keys 16kk .. 16kk+15: columns 8kk .. 8kk+7, low part 32 further.
           const uint32_t pa = base + Cfg::kPCol + 8 * kk;
           tc_mma_ts(base + Cfg::kOCol, pa, bdesc, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          if (Cfg::kSplitP) tc_mma_ts(base + Cfg::kOCol, pa + 32, bdesc, Cfg::kIdescPV, 1u);
+          if (split_p) tc_mma_ts(base + Cfg::kOCol, pa + 32, bdesc, Cfg::kIdescPV, 1u);
         }
         tc_commit(p_free(tt));
       }
@@ -662,6 +668,14 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
               make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
               make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
           pk[KT / 2 + c] = pack_pair<typename Cfg::OpT>(r.x, r.y);
+        } else if (KV8 && split_p) {
+          // fp16 high part rounded to nearest, then the exact remainder
+          // rounded to fp16
+          const __half2 hi = __floats2half2_rn(__uint_as_float(a), __uint_as_float(b));
+          const float2 hf = __half22float2(hi);
+          pk[c] = *reinterpret_cast<const uint32_t*>(&hi);
+          pk[KT / 2 + c] =
+              pack_pair<__half>(__uint_as_float(a) - hf.x, __uint_as_float(b) - hf.y);
         } else {
           pk[c] = pack_pair<typename Cfg::OpT>(__uint_as_float(a), __uint_as_float(b));
           pk[KT / 2 + c] = 0u;

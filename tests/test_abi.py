@@ -113,6 +113,16 @@ def test_block_copy_argument_errors(lib):
     assert lib.paged_block_copy(ctypes.byref(c), P(0x50000), 0, None) == 0
 
 
+def test_read_stream_argument_errors(lib):
+    # Refused on the host, before any CUDA call: null pointers, a buffer or
+    # size that is not a multiple of 16 bytes; an empty buffer launches nothing.
+    assert lib.paged_selftest_read_stream(P(0), 64, P(0x60000), None) == -1
+    assert lib.paged_selftest_read_stream(P(0x50000), 64, P(0), None) == -1
+    assert lib.paged_selftest_read_stream(P(0x50004), 64, P(0x60000), None) == -4
+    assert lib.paged_selftest_read_stream(P(0x50000), 40, P(0x60000), None) == -4
+    assert lib.paged_selftest_read_stream(P(0x50000), 0, P(0x60000), None) == 0
+
+
 def test_workspace_and_partition_sizes(lib):
     c = fake_cache(head_dim=128)
     ref = ctypes.byref(c)

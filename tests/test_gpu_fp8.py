@@ -10,7 +10,7 @@ import torch
 import paged_kv_cache_145_gb300 as pkv
 from oracle import attention as A
 from paged_kv_cache_145_gb300 import synth
-from tests.workload import TOL, edge_tol, fp8_tol, gpu_out_f64
+from tests.workload import TOL, edge_tol, gpu_out_f64
 
 pytestmark = pytest.mark.gpu
 IO = {"f16": torch.float16, "bf16": torch.bfloat16}
@@ -47,10 +47,10 @@ def test_quantizing_write_bit_exact(io, hk, d):
     assert np.array_equal(synth.storage_numpy(cache.v_cache, "e4m3"), ev)
 
 
-def decode_case(io, G, b, d, lens, part, seed, hk=2, q_mult=None, k_scale=None):
+def decode_case(io, G, b, d, lens, part, seed, hk=2, q_mult=None, k_scale=None, v_scale=None):
     nblk = [-(-L // b) for L in lens]
     n = sum(nblk) + 3
-    cache = fp8_cache(n, hk, b, d, io, seed, k_scale=k_scale)
+    cache = fp8_cache(n, hk, b, d, io, seed, k_scale=k_scale, v_scale=v_scale)
     perm = np.random.default_rng(seed).permutation(n)
     tables = np.full((len(lens), max(nblk)), -1, dtype=np.int32)
     pos = 0
@@ -91,6 +91,19 @@ def test_fp8_decode_matches_oracle(io, G, b, d, part, kernel):
     got, ref = decode_case(io, G, b, d, lens, part, seed=hash((io, G, b, d, part)) % 1000)
     assert np.all(np.isfinite(got))
     assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
+
+
+@pytest.mark.parametrize("io,vs,d", [("f16", 3e-3, 128), ("f16", 0.05, 128), ("bf16", 0.012, 128),
+                                     ("bf16", 0.05, 128), ("f16", 0.05, 64)])
+def test_fp8_decode_value_scales_either_side_of_the_split(io, vs, d, kernel):
+    # Values up to 448 * v_scale (22 at 0.05): P enters P.V as one fp16 part
+    # while 2^-11 * 448 * |v_scale| stays within half the output's bar, else
+    # as two parts.  Both forms against the oracle at the stated bars.
+    for seed in range(3):
+        got, ref = decode_case(io, 4, 16, d, [5, 97, 300, 777, 2000], 0, seed=seed,
+                               v_scale=torch.full((2,), vs))
+        assert np.all(np.isfinite(got))
+        assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
 
 
 @pytest.mark.parametrize("io,G,b,d", [("bf16", 4, 16, 128), ("f16", 2, 8, 64)])
@@ -155,11 +168,11 @@ def test_fp8_copy_and_swap_are_byte_moves():
 
 
 def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=None, nan_tail=False,
-                     seqs=None):
+                     seqs=None, v_scale=None):
     lens = [p_ + c for p_, c in zip(prefix, chunk)]
     nblk = [-(-L // b) for L in lens]
     n = sum(nblk) + 3
-    cache = fp8_cache(n, hk, b, 128, io, seed, k_scale=k_scale)
+    cache = fp8_cache(n, hk, b, 128, io, seed, k_scale=k_scale, v_scale=v_scale)
     perm = np.random.default_rng(seed).permutation(n)
     tables = np.full((len(lens), max(nblk) + 1), -1, dtype=np.int32)
     pos = 0
@@ -186,17 +199,26 @@ def fp8_prefill_case(io, G, b, prefix, chunk, seed, hk=2, k_scale=None, q_mult=N
                               synth.storage_numpy(cache.v_cache, "e4m3"), [list(r) for r in tables],
                               lens, starts, scale, b, "e4m3", seqs=seqs, q_dtype=io,
                               k_scale=cache.k_scale.cpu().numpy(), v_scale=cache.v_scale.cpu().numpy())
-    v_max = float(np.nanmax(np.abs(A.dequantize_pool(synth.storage_numpy(cache.v_cache, "e4m3"),
-                                           cache.v_scale.cpu().numpy()))))
-    return gpu_out_f64(out), ref, v_max
+    return gpu_out_f64(out), ref
 
 
 @pytest.mark.parametrize("io,G,b", [("f16", 4, 16), ("bf16", 4, 16), ("bf16", 1, 8), ("f16", 8, 64),
                                     ("bf16", 2, 32)])
 def test_fp8_prefill_matches_oracle(io, G, b):
-    got, ref, vmax = fp8_prefill_case(io, G, b, [0, 5, 100, 17], [37, 64, 3, 130], seed=31 + G + b)
+    got, ref = fp8_prefill_case(io, G, b, [0, 5, 100, 17], [37, 64, 3, 130], seed=31 + G + b)
     assert np.all(np.isfinite(got))
-    assert np.all(np.abs(got - ref) <= fp8_tol(io, ref, vmax))
+    assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
+
+
+@pytest.mark.parametrize("io,vs", [("f16", 3e-3), ("f16", 0.03), ("bf16", 0.012), ("bf16", 0.05)])
+def test_fp8_prefill_value_scales_either_side_of_the_split(io, vs):
+    # P enters P.V as one fp16 part while 2^-11 * 448 * |v_scale| stays
+    # within half the output's bar, else as two parts: both forms against
+    # the oracle at the stated bars, values reaching 448 * v_scale.
+    got, ref = fp8_prefill_case(io, 4, 16, [0, 40, 300], [90, 17, 64], seed=71,
+                                v_scale=torch.full((2,), vs))
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - ref) <= edge_tol(io, ref))
 
 
 def test_fp8_prefill_chunked_workload_full_size_sampled():
@@ -206,23 +228,23 @@ def test_fp8_prefill_chunked_workload_full_size_sampled():
     cfg = synth.CONFIGS["chunked"]
     S, G = cfg["batch"], cfg["heads"] // cfg["kv_heads"]
     chunk = [cfg["chunk"]] * S
-    got, ref, vmax = fp8_prefill_case("bf16", G, cfg["block_size"], [cfg["prefix"]] * S, chunk,
+    got, ref = fp8_prefill_case("bf16", G, cfg["block_size"], [cfg["prefix"]] * S, chunk,
                                       seed=47, hk=cfg["kv_heads"], seqs=[0, S - 1])
     assert np.all(np.isfinite(got))
     rows = np.concatenate([np.arange(0, chunk[0]), np.arange(sum(chunk) - chunk[-1], sum(chunk))])
-    assert np.all(np.abs(got[rows] - ref[rows]) <= fp8_tol("bf16", ref[rows], vmax))
+    assert np.all(np.abs(got[rows] - ref[rows]) <= edge_tol("bf16", ref[rows]))
 
 
 def test_fp8_prefill_bf16_queries_beyond_fp16_range():
-    got, ref, vmax = fp8_prefill_case("bf16", 4, 16, [20, 0], [50, 70], seed=43, q_mult=1e5,
+    got, ref = fp8_prefill_case("bf16", 4, 16, [20, 0], [50, 70], seed=43, q_mult=1e5,
                                       k_scale=torch.full((2,), 3e-7))
     assert np.all(np.isfinite(got))
-    assert np.all(np.abs(got - ref) <= fp8_tol("bf16", ref, vmax))
+    assert np.all(np.abs(got - ref) <= edge_tol("bf16", ref))
 
 
 def test_fp8_prefill_stale_nan_codes():
-    got, ref, vmax = fp8_prefill_case("f16", 4, 16, [3, 0, 40], [5, 17, 9], seed=47, nan_tail=True)
-    assert np.all(np.isfinite(got)) and np.all(np.abs(got - ref) <= fp8_tol("f16", ref, vmax))
+    got, ref = fp8_prefill_case("f16", 4, 16, [3, 0, 40], [5, 17, 9], seed=47, nan_tail=True)
+    assert np.all(np.isfinite(got)) and np.all(np.abs(got - ref) <= edge_tol("f16", ref))
 
 
 def test_fp8_prefill_refusals(monkeypatch):
