@@ -85,6 +85,34 @@ def test_prefill_geometry_grid(dt, D, b, G):
     assert np.all(np.abs(got - ref) <= edge_tol(dt, ref))
 
 
+def test_prefill_bf16_value_magnitudes():
+    # bf16 value tiles whose largest magnitude exceeds 8.192 (where fp16 P
+    # could cost more than half the bar) take the bf16 two-part P path,
+    # tile by tile; values beyond fp16's range (7e4) must not overflow.
+    c = PCase("bf16", 8, 2, 128, 16, [40, 0, 200], [90, 129, 70], seed=23)
+    v = c.v.float()
+    t0 = [int(x) for x in c.tables[0][:3]]          # sequence 0: first 48 positions x 20
+    v[t0] *= 20.0
+    t2 = [int(x) for x in c.tables[2] if x >= 0]    # sequence 2: every value large
+    v[t2] *= 2.0e4
+    v[t2[1], 0, 3, :4] = torch.tensor([7.0e4, -7.0e4, 6.6e4, 1.0e5])
+    c.v = v.to(torch.bfloat16)
+    out, err = c.gpu()
+    assert err == 0
+    got, ref = gpu_out_f64(out), c.oracle()
+    assert np.all(np.isfinite(got))
+    r01 = np.arange(c.starts[0], c.starts[2])
+    assert np.all(np.abs(got[r01] - ref[r01]) <= edge_tol("bf16", ref[r01]))
+    # Sequence 2's values (up to 1e5) are far outside the N(0, 1) data the
+    # stated bars are set for; there the bar is relative to the largest
+    # value: P keeps about 16 bits (2^-16 of each weight) and the output is
+    # rounded once, so 2^-14 * max |v| or one output ulp.
+    r2 = np.arange(c.starts[2], c.starts[3])
+    vmax = float(v[t2].abs().max())
+    bar = np.maximum(edge_tol("bf16", ref[r2]), 2.0 ** -14 * vmax)
+    assert np.all(np.abs(got[r2] - ref[r2]) <= bar)
+
+
 def test_prefill_chunked_workload_full_size_sampled():
     # The benchmark's chunked-prefill workload at full size (8 sequences of
     # 4096 cached positions and a 512-query chunk, GQA 32/8, bf16, block 16)
