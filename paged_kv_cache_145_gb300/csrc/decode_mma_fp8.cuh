@@ -257,114 +257,121 @@ decode_partition_mma_fp8_widen_kernel(const DecodeParams p) {
   unsigned char* vtw = ktw + Cfg::kTileBytes;              // widened values
   const uint32_t ktile = smem_addr(ktw), vtile = smem_addr(vtw);
   uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
-  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);  // the same for the whole CTA
+  // Each CTA uses P as one fp16 part or two (fp8_split_p, the same for the
+  // whole CTA): the chunk loop is compiled once per form and chosen here,
+  // so no per-chunk test of the form stays in it.
+  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);
+  auto chunks = [&](auto split_tag) {
+    constexpr bool SPLIT = decltype(split_tag)::value;
+    int j = 0;
+    for (; j < count; ++j) {
+      const int st = j % NST;
+      timed_out = __any_sync(kFullMask, !mbar_wait(bar0 + st * 8, (uint32_t)((j / NST) & 1)));
+      if (timed_out) break;
+      const int c = warp + j * NW;
+      const int nvalid = min(C, ntok - c * C);
 
-  int j = 0;
-  for (; j < count; ++j) {
-    const int st = j % NST;
-    timed_out = __any_sync(kFullMask, !mbar_wait(bar0 + st * 8, (uint32_t)((j / NST) & 1)));
-    if (timed_out) break;
-    const int c = warp + j * NW;
-    const int nvalid = min(C, ntok - c * C);
-
-    // ---- widen the chunk's codes into the swizzled 16-bit tiles ----------
-    {
-      const unsigned char* raw = smem + Cfg::kRawOff + (warp * NST + st) * Cfg::kRawStage;
-      const int cc = lane % CPR;  // 16-byte code chunk = dims 16cc .. 16cc+15
-#pragma unroll
-      for (int pass = 0; pass < C / RPP; ++pass) {
-        const int r = pass * RPP + lane / CPR;
-        const uint4 kc = *reinterpret_cast<const uint4*>(raw + r * D + cc * 16);
-        const uint4 vc = *reinterpret_cast<const uint4*>(raw + Cfg::kRawBytes + r * D + cc * 16);
-        uint4 k0, k1, v0, v1;
-        widen16<T>(kc, k0, k1);
-        widen16<__half>(vc, v0, v1);
-        if (r >= nvalid) v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
-        const int box = (16 * cc) / 64;
-        const int c8 = ((16 * cc) % 64) / 8;  // first of the two 16-byte chunks
-        unsigned char* kr = ktw + box * Cfg::kBoxBytes + r * 128;
-        unsigned char* vr = vtw + box * Cfg::kBoxBytes + r * 128;
-        *reinterpret_cast<uint4*>(kr + ((c8 ^ (r & 7)) << 4)) = k0;
-        *reinterpret_cast<uint4*>(kr + (((c8 + 1) ^ (r & 7)) << 4)) = k1;
-        *reinterpret_cast<uint4*>(vr + ((c8 ^ (r & 7)) << 4)) = v0;
-        *reinterpret_cast<uint4*>(vr + (((c8 + 1) ^ (r & 7)) << 4)) = v1;
+      // ---- widen the chunk's codes into the swizzled 16-bit tiles ----------
+      {
+        const unsigned char* raw = smem + Cfg::kRawOff + (warp * NST + st) * Cfg::kRawStage;
+        const int cc = lane % CPR;  // 16-byte code chunk = dims 16cc .. 16cc+15
+  #pragma unroll
+        for (int pass = 0; pass < C / RPP; ++pass) {
+          const int r = pass * RPP + lane / CPR;
+          const uint4 kc = *reinterpret_cast<const uint4*>(raw + r * D + cc * 16);
+          const uint4 vc = *reinterpret_cast<const uint4*>(raw + Cfg::kRawBytes + r * D + cc * 16);
+          uint4 k0, k1, v0, v1;
+          widen16<T>(kc, k0, k1);
+          widen16<__half>(vc, v0, v1);
+          if (r >= nvalid) v0 = v1 = make_uint4(0u, 0u, 0u, 0u);
+          const int box = (16 * cc) / 64;
+          const int c8 = ((16 * cc) % 64) / 8;  // first of the two 16-byte chunks
+          unsigned char* kr = ktw + box * Cfg::kBoxBytes + r * 128;
+          unsigned char* vr = vtw + box * Cfg::kBoxBytes + r * 128;
+          *reinterpret_cast<uint4*>(kr + ((c8 ^ (r & 7)) << 4)) = k0;
+          *reinterpret_cast<uint4*>(kr + (((c8 + 1) ^ (r & 7)) << 4)) = k1;
+          *reinterpret_cast<uint4*>(vr + ((c8 ^ (r & 7)) << 4)) = v0;
+          *reinterpret_cast<uint4*>(vr + (((c8 + 1) ^ (r & 7)) << 4)) = v1;
+        }
       }
-    }
-    __syncwarp();
-    if (lane == 0 && j + NST < count) {  // the raw stage is free again
-      fence_proxy_async();
-      issue(j + NST);
-    }
+      __syncwarp();
+      if (lane == 0 && j + NST < count) {  // the raw stage is free again
+        fence_proxy_async();
+        issue(j + NST);
+      }
 
-    // ---- S^T = K . Q^T ----------------------------------------------------
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      const int col8 = 2 * (kk % 4) + k_col8;
-      const uint32_t addr =
-          ktile + (kk / 4) * Cfg::kBoxBytes + k_tok * 128 + ((col8 ^ (k_tok & 7)) << 4);
-      uint32_t a[4];
-      ldsm_x4(a, addr);
-      OpK::run(sc, a, qb[kk][0], qb[kk][1]);
-    }
+      // ---- S^T = K . Q^T ----------------------------------------------------
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+      for (int kk = 0; kk < KSTEPS; ++kk) {
+        const int col8 = 2 * (kk % 4) + k_col8;
+        const uint32_t addr =
+            ktile + (kk / 4) * Cfg::kBoxBytes + k_tok * 128 + ((col8 ^ (k_tok & 7)) << 4);
+        uint32_t a[4];
+        ldsm_x4(a, addr);
+        OpK::run(sc, a, qb[kk][0], qb[kk][1]);
+      }
 
-    // ---- online softmax per head column ------------------------------------
-    const bool v0 = gi < nvalid, v1 = gi + 8 < nvalid;
-    float x[4];
-    x[0] = v0 ? sc[0] * qs : -INFINITY;
-    x[1] = v0 ? sc[1] * qs : -INFINITY;
-    x[2] = v1 ? sc[2] * qs : -INFINITY;
-    x[3] = v1 ? sc[3] * qs : -INFINITY;
-    float alpha[2], pr[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float cm = fmaxf(x[h], x[h + 2]);
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 4));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 8));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 16));
-      const float mnew = fmaxf(m[h], cm);
-      alpha[h] = exp2f(m[h] - mnew);
-      pr[h] = exp2f(x[h] - mnew);
-      pr[h + 2] = exp2f(x[h + 2] - mnew);
-      float cs = pr[h] + pr[h + 2];
-      cs += __shfl_xor_sync(kFullMask, cs, 4);
-      cs += __shfl_xor_sync(kFullMask, cs, 8);
-      cs += __shfl_xor_sync(kFullMask, cs, 16);
-      l[h] = l[h] * alpha[h] + cs;
-      m[h] = mnew;
-    }
-    if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
+      // ---- online softmax per head column ------------------------------------
+      const bool v0 = gi < nvalid, v1 = gi + 8 < nvalid;
+      float x[4];
+      x[0] = v0 ? sc[0] * qs : -INFINITY;
+      x[1] = v0 ? sc[1] * qs : -INFINITY;
+      x[2] = v1 ? sc[2] * qs : -INFINITY;
+      x[3] = v1 ? sc[3] * qs : -INFINITY;
+      float alpha[2], pr[4];
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float cm = fmaxf(x[h], x[h + 2]);
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 4));
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 8));
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 16));
+        const float mnew = fmaxf(m[h], cm);
+        alpha[h] = exp2f(m[h] - mnew);
+        pr[h] = exp2f(x[h] - mnew);
+        pr[h + 2] = exp2f(x[h + 2] - mnew);
+        float cs = pr[h] + pr[h + 2];
+        cs += __shfl_xor_sync(kFullMask, cs, 4);
+        cs += __shfl_xor_sync(kFullMask, cs, 8);
+        cs += __shfl_xor_sync(kFullMask, cs, 16);
+        l[h] = l[h] * alpha[h] + cs;
+        m[h] = mnew;
+      }
+      if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
+  #pragma unroll
+        for (int i = 0; i < KSTEPS; ++i) {
+          acc[i][0] *= alpha[0];
+          acc[i][1] *= alpha[1];
+          acc[i][2] *= alpha[0];
+          acc[i][3] *= alpha[1];
+        }
+      }
+
+      // ---- P^T (fp16) through shared memory ---------------------------------
+      stage_pt<C>(pt, gi, ti, pr, SPLIT);
+      __syncwarp();
+      const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
+      const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
+      const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
+      const uint32_t b0l = SPLIT ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
+      const uint32_t b1l = SPLIT ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
+
+      // ---- O^T += V^T . P^T (fp16; low part too when split) -------------------
+  #pragma unroll
       for (int i = 0; i < KSTEPS; ++i) {
-        acc[i][0] *= alpha[0];
-        acc[i][1] *= alpha[1];
-        acc[i][2] *= alpha[0];
-        acc[i][3] *= alpha[1];
+        const int col8 = 2 * (i % 4) + v_col8;
+        const uint32_t addr =
+            vtile + (i / 4) * Cfg::kBoxBytes + v_tok * 128 + ((col8 ^ (v_tok & 7)) << 4);
+        uint32_t a[4];
+        ldsm_x4_trans(a, addr);
+        OpV::run(acc[i], a, b0, b1);
+        if constexpr (SPLIT) OpV::run(acc[i], a, b0l, b1l);
       }
+      __syncwarp();  // the widened tiles and P^T are rewritten next chunk
     }
-
-    // ---- P^T (fp16) through shared memory ---------------------------------
-    stage_pt<C>(pt, gi, ti, pr, split_p);
-    __syncwarp();
-    const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
-    const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
-    const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
-    const uint32_t b0l = split_p ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
-    const uint32_t b1l = split_p ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
-
-    // ---- O^T += V^T . P^T (fp16; low part too when split) -------------------
-#pragma unroll
-    for (int i = 0; i < KSTEPS; ++i) {
-      const int col8 = 2 * (i % 4) + v_col8;
-      const uint32_t addr =
-          vtile + (i / 4) * Cfg::kBoxBytes + v_tok * 128 + ((col8 ^ (v_tok & 7)) << 4);
-      uint32_t a[4];
-      ldsm_x4_trans(a, addr);
-      OpV::run(acc[i], a, b0, b1);
-      if (split_p) OpV::run(acc[i], a, b0l, b1l);
-    }
-    __syncwarp();  // the widened tiles and P^T are rewritten next chunk
-  }
+    return j;
+  };
+  const int j = split_p ? chunks(std::true_type{}) : chunks(std::false_type{});
   if (timed_out) {
     const int last = count < j + NST ? count : j + NST;
     for (int jj = j + 1; jj < last; ++jj)
@@ -607,118 +614,125 @@ decode_partition_mma_fp8_kernel(const DecodeParams p, const __grid_constant__ CU
   const int k_row = (mm & 1) * 8 + mr;  // ldmatrix row this lane addresses (keys)
   const int k_half = mm >> 1;           // which 16-code chunk of the pair
   uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
-  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);  // the same for the whole CTA
+  // Each CTA uses P as one fp16 part or two (fp8_split_p, the same for the
+  // whole CTA): the chunk loop is compiled once per form and chosen here,
+  // so no per-chunk test of the form stays in it.
+  const bool split_p = fp8_split_p<T>(p.v_scale[kvh]);
+  auto chunks = [&](auto split_tag) {
+    constexpr bool SPLIT = decltype(split_tag)::value;
+    int j = 0;
+    for (; j < count; ++j) {
+      const int st = j % NST;
+      timed_out = __any_sync(kFullMask, !mbar_wait(bar0 + st * 8, (uint32_t)((j / NST) & 1)));
+      if (timed_out) break;
+      const int c = warp + j * NW;
+      const int nvalid = min(C, ntok - c * C);
+      const uint32_t kraw = raw0 + st * Cfg::kRawStage;
+      const unsigned char* vraw = smem + (kraw - smem_addr(smem)) + Cfg::kRawBytes;
 
-  int j = 0;
-  for (; j < count; ++j) {
-    const int st = j % NST;
-    timed_out = __any_sync(kFullMask, !mbar_wait(bar0 + st * 8, (uint32_t)((j / NST) & 1)));
-    if (timed_out) break;
-    const int c = warp + j * NW;
-    const int nvalid = min(C, ntok - c * C);
-    const uint32_t kraw = raw0 + st * Cfg::kRawStage;
-    const unsigned char* vraw = smem + (kraw - smem_addr(smem)) + Cfg::kRawBytes;
-
-    // ---- S^T = K . Q^T, key fragments straight from the codes -------------
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kp = 0; kp < KSTEPS / 2; ++kp) {  // two k-steps (32 codes) per ldmatrix
-      const int chunk = 2 * kp + k_half;
-      uint32_t r[4];
-      ldsm_x4(r, kraw + k_row * 128 + ((chunk ^ (k_row & 7)) << 4));
-      // r[0]: row gi, 4 codes of chunk 2kp; r[1]: row gi+8; r[2], r[3]: chunk 2kp+1.
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t a[4];
-        e4m3x4_to_f16x4(r[2 * h], a[0], a[2]);
-        e4m3x4_to_f16x4(r[2 * h + 1], a[1], a[3]);
-        Op::run(sc, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
-      }
-    }
-
-    // ---- online softmax per head column ------------------------------------
-    const bool v0 = gi < nvalid, v1 = gi + 8 < nvalid;
-    float x[4];
-    x[0] = v0 ? sc[0] * qs : -INFINITY;
-    x[1] = v0 ? sc[1] * qs : -INFINITY;
-    x[2] = v1 ? sc[2] * qs : -INFINITY;
-    x[3] = v1 ? sc[3] * qs : -INFINITY;
-    float alpha[2], pr[4];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float cm = fmaxf(x[h], x[h + 2]);
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 4));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 8));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 16));
-      const float mnew = fmaxf(m[h], cm);
-      alpha[h] = exp2f(m[h] - mnew);
-      pr[h] = exp2f(x[h] - mnew);
-      pr[h + 2] = exp2f(x[h + 2] - mnew);
-      float cs = pr[h] + pr[h + 2];
-      cs += __shfl_xor_sync(kFullMask, cs, 4);
-      cs += __shfl_xor_sync(kFullMask, cs, 8);
-      cs += __shfl_xor_sync(kFullMask, cs, 16);
-      l[h] = l[h] * alpha[h] + cs;
-      m[h] = mnew;
-    }
-    if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-      for (int i = 0; i < KSTEPS; ++i) {
-        acc[i][0] *= alpha[0];
-        acc[i][1] *= alpha[1];
-        acc[i][2] *= alpha[0];
-        acc[i][3] *= alpha[1];
-      }
-    }
-    stage_pt<C>(pt, gi, ti, pr, split_p);
-    __syncwarp();
-    const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
-    const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
-    const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
-    const uint32_t b0l = split_p ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
-    const uint32_t b1l = split_p ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
-
-    // ---- O^T += V^T . P^T, value fragments straight from the codes --------
-    // The contraction runs over positions, which sit in different code rows,
-    // so each lane gathers a 4 x 4 byte block: dims 4w .. 4w+3 (w = gi + 8q)
-    // of rows 2ti, 2ti+1, 2ti+8, 2ti+9 (four 32-bit loads that hit 32
-    // distinct banks under the 128-byte swizzle), pairs the bytes of two
-    // rows per dim with byte permutes and widens them to fp16.  The M rows
-    // of the two tiles of group q are dims 4w, 4w+1 (tile 2q) and 4w+2,
-    // 4w+3 (tile 2q+1); the merge below undoes that order.
-    {
-      const int r0 = 2 * ti;
-      const bool ok0 = r0 < nvalid, ok1 = r0 + 1 < nvalid, ok2 = r0 + 8 < nvalid,
-                 ok3 = r0 + 9 < nvalid;
-#pragma unroll
-      for (int q = 0; q < D / 32; ++q) {
-        const int w = gi + 8 * q;
-        const int ch = w >> 2, wo = (w & 3) * 4;
-        auto word = [&](int r, bool ok) -> uint32_t {
-          return ok ? *reinterpret_cast<const uint32_t*>(vraw + r * 128 + ((ch ^ (r & 7)) << 4) + wo)
-                    : 0u;
-        };
-        const uint32_t x0 = word(r0, ok0), x1 = word(r0 + 1, ok1);
-        const uint32_t x2 = word(r0 + 8, ok2), x3 = word(r0 + 9, ok3);
-        uint32_t a[4], b[4];
-        e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x5140), a[0], a[1]);
-        e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x5140), a[2], a[3]);
-        e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x7362), b[0], b[1]);
-        e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x7362), b[2], b[3]);
-        Op::run(acc[2 * q], a, b0, b1);
-        Op::run(acc[2 * q + 1], b, b0, b1);
-        if (split_p) {
-          Op::run(acc[2 * q], a, b0l, b1l);
-          Op::run(acc[2 * q + 1], b, b0l, b1l);
+      // ---- S^T = K . Q^T, key fragments straight from the codes -------------
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  #pragma unroll
+      for (int kp = 0; kp < KSTEPS / 2; ++kp) {  // two k-steps (32 codes) per ldmatrix
+        const int chunk = 2 * kp + k_half;
+        uint32_t r[4];
+        ldsm_x4(r, kraw + k_row * 128 + ((chunk ^ (k_row & 7)) << 4));
+        // r[0]: row gi, 4 codes of chunk 2kp; r[1]: row gi+8; r[2], r[3]: chunk 2kp+1.
+  #pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t a[4];
+          e4m3x4_to_f16x4(r[2 * h], a[0], a[2]);
+          e4m3x4_to_f16x4(r[2 * h + 1], a[1], a[3]);
+          Op::run(sc, a, qb[2 * kp + h][0], qb[2 * kp + h][1]);
         }
       }
+
+      // ---- online softmax per head column ------------------------------------
+      const bool v0 = gi < nvalid, v1 = gi + 8 < nvalid;
+      float x[4];
+      x[0] = v0 ? sc[0] * qs : -INFINITY;
+      x[1] = v0 ? sc[1] * qs : -INFINITY;
+      x[2] = v1 ? sc[2] * qs : -INFINITY;
+      x[3] = v1 ? sc[3] * qs : -INFINITY;
+      float alpha[2], pr[4];
+  #pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float cm = fmaxf(x[h], x[h + 2]);
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 4));
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 8));
+        cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 16));
+        const float mnew = fmaxf(m[h], cm);
+        alpha[h] = exp2f(m[h] - mnew);
+        pr[h] = exp2f(x[h] - mnew);
+        pr[h + 2] = exp2f(x[h + 2] - mnew);
+        float cs = pr[h] + pr[h + 2];
+        cs += __shfl_xor_sync(kFullMask, cs, 4);
+        cs += __shfl_xor_sync(kFullMask, cs, 8);
+        cs += __shfl_xor_sync(kFullMask, cs, 16);
+        l[h] = l[h] * alpha[h] + cs;
+        m[h] = mnew;
+      }
+      if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
+  #pragma unroll
+        for (int i = 0; i < KSTEPS; ++i) {
+          acc[i][0] *= alpha[0];
+          acc[i][1] *= alpha[1];
+          acc[i][2] *= alpha[0];
+          acc[i][3] *= alpha[1];
+        }
+      }
+      stage_pt<C>(pt, gi, ti, pr, SPLIT);
+      __syncwarp();
+      const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
+      const uint32_t b0 = ptw[(gi * C + 2 * ti) / 2];
+      const uint32_t b1 = ptw[(gi * C + 2 * ti + 8) / 2];
+      const uint32_t b0l = SPLIT ? ptw[(8 * C + gi * C + 2 * ti) / 2] : 0u;
+      const uint32_t b1l = SPLIT ? ptw[(8 * C + gi * C + 2 * ti + 8) / 2] : 0u;
+
+      // ---- O^T += V^T . P^T, value fragments straight from the codes --------
+      // The contraction runs over positions, which sit in different code rows,
+      // so each lane gathers a 4 x 4 byte block: dims 4w .. 4w+3 (w = gi + 8q)
+      // of rows 2ti, 2ti+1, 2ti+8, 2ti+9 (four 32-bit loads that hit 32
+      // distinct banks under the 128-byte swizzle), pairs the bytes of two
+      // rows per dim with byte permutes and widens them to fp16.  The M rows
+      // of the two tiles of group q are dims 4w, 4w+1 (tile 2q) and 4w+2,
+      // 4w+3 (tile 2q+1); the merge below undoes that order.
+      {
+        const int r0 = 2 * ti;
+        const bool ok0 = r0 < nvalid, ok1 = r0 + 1 < nvalid, ok2 = r0 + 8 < nvalid,
+                   ok3 = r0 + 9 < nvalid;
+  #pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+          const int w = gi + 8 * q;
+          const int ch = w >> 2, wo = (w & 3) * 4;
+          auto word = [&](int r, bool ok) -> uint32_t {
+            return ok ? *reinterpret_cast<const uint32_t*>(vraw + r * 128 + ((ch ^ (r & 7)) << 4) + wo)
+                      : 0u;
+          };
+          const uint32_t x0 = word(r0, ok0), x1 = word(r0 + 1, ok1);
+          const uint32_t x2 = word(r0 + 8, ok2), x3 = word(r0 + 9, ok3);
+          uint32_t a[4], b[4];
+          e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x5140), a[0], a[1]);
+          e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x5140), a[2], a[3]);
+          e4m3x4_to_f16x4(__byte_perm(x0, x1, 0x7362), b[0], b[1]);
+          e4m3x4_to_f16x4(__byte_perm(x2, x3, 0x7362), b[2], b[3]);
+          Op::run(acc[2 * q], a, b0, b1);
+          Op::run(acc[2 * q + 1], b, b0, b1);
+          if constexpr (SPLIT) {
+            Op::run(acc[2 * q], a, b0l, b1l);
+            Op::run(acc[2 * q + 1], b, b0l, b1l);
+          }
+        }
+      }
+      __syncwarp();  // the raw stage and P^T are rewritten next
+      if (lane == 0 && j + NST < count) {  // raw stage consumed: refill it
+        fence_proxy_async();
+        issue(j + NST);
+      }
     }
-    __syncwarp();  // the raw stage and P^T are rewritten next
-    if (lane == 0 && j + NST < count) {  // raw stage consumed: refill it
-      fence_proxy_async();
-      issue(j + NST);
-    }
-  }
+    return j;
+  };
+  const int j = split_p ? chunks(std::true_type{}) : chunks(std::false_type{});
   if (timed_out) {
     const int last = count < j + NST ? count : j + NST;
     for (int jj = j + 1; jj < last; ++jj)
