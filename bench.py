@@ -56,13 +56,13 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 # dtype and partition length, with the hash of the sources of that kernel
 # family they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b/native/512": (1280424472, "118000bf3980d6e6"),
-    "gqa/native/512": (1129142640, "118000bf3980d6e6"),
-    "opt13b/fp8/2048": (644210176, "a67ff3c59e9fdaf1"),
-    "gqa/fp8/2048": (565904896, "a67ff3c59e9fdaf1"),
-    "long/native/512": (877668096, "118000bf3980d6e6"),
-    "long/fp8/1536": (439782912, "a67ff3c59e9fdaf1"),
-    "fork/native/512": (79609344, "118000bf3980d6e6"),
+    "opt13b/native/512": (1277883392, "212a013fc36964d1"),
+    "gqa/native/512": (1127114752, "212a013fc36964d1"),
+    "opt13b/fp8/2048": (641348352, "fc43370ae5b670a4"),
+    "gqa/fp8/2048": (563023616, "fc43370ae5b670a4"),
+    "long/native/512": (875519232, "212a013fc36964d1"),
+    "long/fp8/1536": (437342976, "fc43370ae5b670a4"),
+    "fork/native/512": (77156608, "212a013fc36964d1"),
 }
 
 KERNEL_SOURCES = {
