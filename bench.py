@@ -838,16 +838,31 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
     scale = 1.0 / math.sqrt(w.D)
     has_pairs = len(w.pairs) > 0
     nparts_max = -(-w.max_len // part)
-    decode_launches = 1 + (1 if nparts_max > 1 else 0)
+    shared = name == "fork" and args.decode == "shared"
+    decode_launches = 1 + (1 if nparts_max > 1 else 0) + (1 if shared else 0)
     launches_per_step = 1 + decode_launches + (1 if has_pairs else 0)
 
     stream = torch.cuda.current_stream()
 
     resident = (q, k, v, slots, tables, lens, pairs)
 
+    # Forked batches (the parallel-sampling workload) decode their shared
+    # prompt once per group with the shared-prefix entry point; --decode
+    # plain times the plain decode instead.
+    if shared:
+        groups, forks = w.cfg["groups"], w.cfg["forks"]
+        g_starts = torch.arange(0, groups * forks + 1, forks, dtype=torch.int32, device=dev)
+        g_prefix = torch.full((groups,), (w.cfg["prompt"] // w.b) * w.b, dtype=torch.int32,
+                              device=dev)
+
     def decode(x=resident, o=out):
-        pkv.paged_attention_decode(cache, x[0], x[4], x[5], scale, out=o, max_seq_len=w.max_len,
-                                   workspace=ws, partition_size=part)
+        if shared:
+            pkv.paged_attention_decode_shared(cache, x[0], x[4], x[5], scale, g_starts, g_prefix,
+                                              forks, out=o, max_seq_len=w.max_len, workspace=ws,
+                                              partition_size=part)
+        else:
+            pkv.paged_attention_decode(cache, x[0], x[4], x[5], scale, out=o,
+                                       max_seq_len=w.max_len, workspace=ws, partition_size=part)
 
     def step(x=resident, o=out):
         if has_pairs:
@@ -996,6 +1011,9 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
                    "kv_dtype": w.kv_dtype,
                    "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
                    "pool_blocks": w.N, "partition_size": part, "table": w.table_kind,
+                   "decode": ("shared prefix: %d groups of %d forks, %d positions shared"
+                              % (w.cfg["groups"], w.cfg["forks"], (w.cfg["prompt"] // w.b) * w.b)
+                              if shared else "plain"),
                    "slot_utilization": round(w.utilization, 5),
                    "l2": ("flushed before every timed step (pool %.1f MB < 2 x L2 %.0f MB)"
                           % (w.pool_bytes() / 1e6, l2_bytes / 1e6) if flush_l2 else
@@ -1013,7 +1031,9 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
                     "(no projections, MLP or sampling)" % layers},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "paged_attention_decode (partition pass + split-K merge)",
+                     "kernel": ("paged_attention_decode_shared (shared-prefix pass + partition "
+                                "pass + split-K merge)" if shared else
+                                "paged_attention_decode (partition pass + split-K merge)"),
                      "peak_source": peak_kind,
                      "peak_note": ("the measured device-to-device copy rate (half reads, half "
                                    "writes); decode only reads, so it can exceed 1.0"),
@@ -1362,6 +1382,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-all-cores", action="store_true",
                     help="skip the all-cores oracle figure beside the one-process one")
+    ap.add_argument("--decode", choices=("shared", "plain"), default="shared",
+                    help="forked workload: shared-prefix decode (default) or the plain decode")
     ap.add_argument("--no-gqa", action="store_true",
                     help="default line: skip the GQA workload's sub-record")
     args = ap.parse_args()

@@ -78,6 +78,8 @@ typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dt
 #define PKV_DEV_SEQ_LEN      4u  /* decode: length not in [1, max_seq_len]        */
 #define PKV_DEV_PAIR_RANGE   8u  /* paged_block_copy: src or dst not in [0, N)    */
 #define PKV_DEV_TIMEOUT     16u  /* a bounded wait for a bulk copy gave up        */
+#define PKV_DEV_SHARING     32u  /* shared-prefix decode: a member's table or     */
+                                 /* length disagrees with its group's prefix      */
 /* After PKV_DEV_TIMEOUT the launch that set it may have ended with bulk
  * copies still in flight into its shared memory (the drain after a timeout
  * is itself bounded).  Treat the stream as failed: that launch's outputs,
@@ -237,6 +239,48 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
                             const int32_t* block_tables, int32_t max_blocks_per_seq,
                             const int32_t* seq_lens, int32_t num_heads, float scale, void* out,
                             cudaStream_t stream);
+
+/*
+ * paged_attention_decode_shared -- paged_attention_decode for batches in
+ * which groups of sequences share the first blocks of their tables (forks
+ * of one prompt: parallel sampling, beam search).  [VM-LLM] sharing
+ * paragraph: branches of one prompt share its KV blocks; [vLLM-TGI] "Exact
+ * CPU block manager and copy-on-write": a fork shares every block of its
+ * parent until a write needs a private copy.
+ *
+ * Same output as paged_attention_decode.  The partitions (of
+ * partition_size positions) that lie wholly inside a group's shared prefix
+ * are computed once per (group, KV head) for all members' queries
+ * together, so each shared page is read once instead of once per member;
+ * the rest of each sequence is decoded as usual and merged with them.
+ *
+ *   group_starts   device int32[num_groups + 1]: group g is the sequences
+ *                  group_starts[g] .. group_starts[g+1] - 1 (consecutive,
+ *                  ascending).  Sequences outside every group are decoded
+ *                  in full.
+ *   group_prefix   device int32[num_groups]: positions 0 .. prefix - 1 of
+ *                  every member are shared: each member's table names the
+ *                  group's first member's blocks for them, and each
+ *                  member's length is at least prefix.
+ *   max_group_size host bound on group sizes (1 .. num_seqs).
+ *   workspace      as for paged_attention_decode (same size).
+ *
+ * A member whose table or length breaks its group's contract gets a zero
+ * output row and sets PKV_DEV_SHARING.  Groups apply to fp16 and bf16
+ * pools; other pools decode every sequence in full (the same attention).
+ * num_groups = 0 is plain decode.  Host errors as for
+ * paged_attention_decode, plus PKV_ERR_ARG for num_groups outside
+ * [0, 65535] or max_group_size outside [1, num_seqs], PKV_ERR_NULL /
+ * PKV_ERR_ALIGN for the group arrays.
+ */
+int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                  int32_t max_seq_len, float scale, void* out,
+                                  const int32_t* group_starts, const int32_t* group_prefix,
+                                  int32_t num_groups, int32_t max_group_size, void* workspace,
+                                  size_t workspace_bytes, int32_t partition_size,
+                                  cudaStream_t stream);
 
 /*
  * paged_attention_decode_static_ws -- paged_attention_decode without a

@@ -29,7 +29,8 @@ __all__ = [
     "paged_attention_prefill",
     "paged_attention_workspace_bytes", "paged_attention_partition_size",
     "paged_block_copy", "paged_block_swap", "paged_get_device_error",
-    "paged_selftest_wait_timeout", "paged_selftest_read_stream", "library_path",
+    "paged_selftest_wait_timeout", "paged_selftest_read_stream", "paged_attention_decode_shared",
+    "library_path",
 ]
 
 
@@ -165,6 +166,49 @@ def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, ma
         cache.ref, _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
         num_heads, max_seq_len, float(scale), _ptr(out), ws_ptr, ws_len, partition_size,
         _stream(stream)), "paged_attention_decode")
+    return out
+
+
+def paged_attention_decode_shared(cache, q, block_tables, seq_lens, scale, group_starts,
+                                  group_prefix, max_group_size, out=None, max_seq_len=0,
+                                  workspace=None, partition_size=0, stream=None):
+    """Decode attention like :func:`paged_attention_decode` for a batch whose
+    groups of consecutive sequences share a table prefix.
+
+    ``group_starts``: int32 ``[num_groups + 1]`` (group g is sequences
+    ``group_starts[g] .. group_starts[g+1] - 1``); ``group_prefix``: int32
+    ``[num_groups]`` positions shared by every member; ``max_group_size``:
+    host bound on group sizes.  Returns ``out``.
+    """
+    _need(q, "q", cache.io_dtype, cache.device)
+    _need(block_tables, "block_tables", torch.int32, cache.device)
+    _need(seq_lens, "seq_lens", torch.int32, cache.device)
+    _need(group_starts, "group_starts", torch.int32, cache.device)
+    _need(group_prefix, "group_prefix", torch.int32, cache.device)
+    if q.dim() != 3 or q.shape[2] != cache.head_dim:
+        raise ValueError("q must be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads = q.shape[0], q.shape[1]
+    if block_tables.dim() != 2 or block_tables.shape[0] != num_seqs or seq_lens.shape != (num_seqs,):
+        raise ValueError("block_tables must be [num_seqs, max_blocks] and seq_lens [num_seqs]")
+    num_groups = group_prefix.numel()
+    if group_starts.numel() != num_groups + 1:
+        raise ValueError("group_starts must hold num_groups + 1 entries")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", cache.io_dtype, cache.device)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    bound = max_seq_len if max_seq_len else block_tables.shape[1] * cache.block_size
+    need = paged_attention_workspace_bytes(cache, num_seqs, num_heads, bound, partition_size)
+    if need and workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=cache.device)
+    ws_ptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    ws_len = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _lib.check(_lib.lib().paged_attention_decode_shared(
+        cache.ref, _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
+        num_heads, max_seq_len, float(scale), _ptr(out), _ptr(group_starts), _ptr(group_prefix),
+        num_groups, int(max_group_size), ws_ptr, ws_len, partition_size, _stream(stream)),
+        "paged_attention_decode_shared")
     return out
 
 

@@ -38,6 +38,10 @@ int pkv_launch_decode_f16(const pkv::DecodeParams&, int, int, int, int, const pk
                           cudaStream_t);
 int pkv_launch_decode_bf16(const pkv::DecodeParams&, int, int, int, int, const pkv::DecodeMaps*,
                            cudaStream_t);
+int pkv_launch_decode_shared_f16(const pkv::DecodeParams&, int, int, int, int, int,
+                                 const pkv::DecodeMaps*, const pkv::DecodeMaps*, cudaStream_t);
+int pkv_launch_decode_shared_bf16(const pkv::DecodeParams&, int, int, int, int, int,
+                                  const pkv::DecodeMaps*, const pkv::DecodeMaps*, cudaStream_t);
 
 // One error word per device, OR-ed by the kernels (PKV_DEV_* bits).
 static __device__ unsigned g_pkv_error;
@@ -260,11 +264,15 @@ size_t paged_attention_workspace_bytes(const pkv_cache* cache, int32_t num_seqs,
   return workspace_layout(num_seqs, num_heads, cache->head_dim, max_seq_len, part).total;
 }
 
-int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t* block_tables,
-                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
-                           int32_t num_heads, int32_t max_seq_len, float scale, void* out,
-                           void* workspace, size_t workspace_bytes, int32_t partition_size,
-                           cudaStream_t stream) {
+namespace {
+
+// Decode, plain (no groups) or with shared-prefix groups.
+int decode_impl(const pkv_cache* cache, const void* q, const int32_t* block_tables,
+                int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                int32_t num_heads, int32_t max_seq_len, float scale, void* out,
+                const int32_t* group_starts, const int32_t* group_prefix, int32_t num_groups,
+                int32_t max_group_size, void* workspace, size_t workspace_bytes,
+                int32_t partition_size, cudaStream_t stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
   rc = check_scales(cache);
@@ -313,7 +321,31 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
   p.err = err;
   p.k_scale = cache->k_scale;
   p.v_scale = cache->v_scale;
+  p.num_seqs = num_seqs;
   const int group = num_heads / cache->num_kv_heads;
+  // Shared-prefix groups run on 16-bit pools (the grouped kernel's
+  // tensor-core tiles); other pools decode every sequence in full, which
+  // gives the same attention.
+  const bool shared = group_starts && num_groups > 0 &&
+                      (cache->dtype == PKV_F16 || cache->dtype == PKV_BF16);
+  if (shared) {
+    pkv::DecodeMaps maps;
+    if (!encode_pool_map(&maps.k, cache, cache->k_cache) ||
+        !encode_pool_map(&maps.v, cache, cache->v_cache))
+      return PKV_ERR_CUDA;
+    p.group_starts = group_starts;
+    p.group_prefix = group_prefix;
+    p.num_groups = num_groups;
+    const int D = cache->head_dim, B = cache->block_size;
+    // The partition pass takes the tensor-core kernel only where the plain
+    // decode would; the shared-prefix kernel always reads through the maps.
+    const pkv::DecodeMaps* mp = use_mma(cache, group) ? &maps : nullptr;
+    return cache->dtype == PKV_F16
+               ? pkv_launch_decode_shared_f16(p, num_seqs, D, B, group, max_group_size, &maps, mp,
+                                              stream)
+               : pkv_launch_decode_shared_bf16(p, num_seqs, D, B, group, max_group_size, &maps,
+                                               mp, stream);
+  }
   if (cache->dtype == PKV_FP8_E4M3) {
     const bool mma = use_mma(cache, group);
     pkv::DecodeMaps fmaps;
@@ -342,6 +374,38 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
     case PKV_BF16: return pkv_launch_decode_bf16(p, num_seqs, D, B, group, mp, stream);
   }
   return PKV_ERR_ARG;
+}
+
+}  // namespace
+
+int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
+                           int32_t num_heads, int32_t max_seq_len, float scale, void* out,
+                           void* workspace, size_t workspace_bytes, int32_t partition_size,
+                           cudaStream_t stream) {
+  return decode_impl(cache, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
+                     max_seq_len, scale, out, nullptr, nullptr, 0, 0, workspace, workspace_bytes,
+                     partition_size, stream);
+}
+
+int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
+                                  const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                  const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
+                                  int32_t max_seq_len, float scale, void* out,
+                                  const int32_t* group_starts, const int32_t* group_prefix,
+                                  int32_t num_groups, int32_t max_group_size, void* workspace,
+                                  size_t workspace_bytes, int32_t partition_size,
+                                  cudaStream_t stream) {
+  if (num_groups < 0 || num_groups > 65535 || (num_groups > 0 && (max_group_size < 1 ||
+                                                                  max_group_size > num_seqs)))
+    return PKV_ERR_ARG;
+  if (num_groups > 0 && (!group_starts || !group_prefix)) return PKV_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(group_starts) & 3u) ||
+      (reinterpret_cast<uintptr_t>(group_prefix) & 3u))
+    return PKV_ERR_ALIGN;
+  return decode_impl(cache, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
+                     max_seq_len, scale, out, group_starts, group_prefix, num_groups,
+                     max_group_size, workspace, workspace_bytes, partition_size, stream);
 }
 
 int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total_queries,

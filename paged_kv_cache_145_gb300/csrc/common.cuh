@@ -58,6 +58,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// One plain arrival (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Non-blocking test of the same condition (never suspends the thread), for
 // roles that poll several barriers.
 __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {

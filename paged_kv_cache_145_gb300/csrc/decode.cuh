@@ -72,7 +72,39 @@ struct DecodeParams {
   unsigned* err;
   const float* k_scale;  // FP8 pools: per-KV-head scales (else unused)
   const float* v_scale;
+  // Shared-prefix decode (null otherwise): groups of consecutive sequences
+  // [group_starts[g], group_starts[g+1]) whose first group_prefix[g]
+  // positions are shared; the partitions inside that prefix are computed by
+  // decode_shared_prefix_kernel, and the partition pass skips them.
+  const int32_t* group_starts;
+  const int32_t* group_prefix;
+  int num_groups;
+  int num_seqs;
 };
+
+// Group owning sequence s, or -1: the last g with group_starts[g] <= s,
+// provided s < group_starts[g+1].  The shared-prefix kernel and the
+// partition pass both use this rule, so a malformed group list can leave a
+// sequence without a group (decoded plainly) but never covered twice.
+__device__ __forceinline__ int shared_owner(const DecodeParams& p, int s) {
+  if (!p.group_starts || p.num_groups <= 0) return -1;
+  int lo = 0, hi = p.num_groups - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (ld_nc(p.group_starts + mid) <= s) lo = mid;
+    else hi = mid - 1;
+  }
+  const int a = ld_nc(p.group_starts + lo), b = ld_nc(p.group_starts + lo + 1);
+  return (a <= s && s < b) ? lo : -1;
+}
+
+// Partitions of sequence s that the shared-prefix kernel computes.
+__device__ __forceinline__ int shared_parts_of(const DecodeParams& p, int s) {
+  const int g = shared_owner(p, s);
+  if (g < 0) return 0;
+  const int pre = ld_nc(p.group_prefix + g);
+  return pre > 0 ? pre / p.part_size : 0;
+}
 
 constexpr int kMaxPartSize = 8192;
 
@@ -179,6 +211,8 @@ decode_partition_kernel(const DecodeParams p) {
     return;
   }
   if (tok0 >= L) return;
+  // Partitions inside a shared prefix are the shared-prefix kernel's.
+  if (part < shared_parts_of(p, s)) return;
   const int ntok = min(L - tok0, PS);
   const int nparts = (L + PS - 1) / PS;
   const int nblk = (ntok + BS - 1) / BS;

@@ -6,3 +6,11 @@ int pkv_launch_decode_bf16(const pkv::DecodeParams& p, int num_seqs, int head_di
                         int group, const pkv::DecodeMaps* maps, cudaStream_t stream) {
   return pkv::launch_decode<__nv_bfloat16>(p, num_seqs, head_dim, block_size, group, maps, stream);
 }
+
+int pkv_launch_decode_shared_bf16(const pkv::DecodeParams& p, int num_seqs, int head_dim,
+                               int block_size, int group, int max_group_size,
+                               const pkv::DecodeMaps* maps, const pkv::DecodeMaps* part_maps,
+                               cudaStream_t stream) {
+  return pkv::launch_decode_shared<__nv_bfloat16>(p, num_seqs, head_dim, block_size, group, max_group_size,
+                                        maps, part_maps, stream);
+}

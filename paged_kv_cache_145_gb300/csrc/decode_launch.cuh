@@ -9,6 +9,7 @@
 #include "decode.cuh"
 #include "decode_mma.cuh"
 #include "decode_mma_fp8.cuh"
+#include "decode_shared.cuh"
 
 namespace pkv {
 
@@ -75,6 +76,40 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* map
   }
   launch_reduce<T, D>(p, num_seqs, stream);
   return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Shared-prefix decode (16-bit pools): the groups' shared partitions, then
+// the partition pass over the rest and the merge.
+// `maps` feed the shared-prefix kernel; `part_maps` (null: CUDA-core
+// kernel) the partition pass, as in the plain decode.
+template <typename T, int D, int BS, int G>
+int launch_shared_cfg(const DecodeParams& p, int num_seqs, int max_group_size,
+                      const DecodeMaps* maps, const DecodeMaps* part_maps, cudaStream_t stream) {
+  using Cfg = SharedCfg<T, D, BS, G>;
+  const int64_t row_blocks = ((int64_t)max_group_size * G + Cfg::kRows - 1) / Cfg::kRows;
+  if ((int64_t)p.num_parts * row_blocks > 65535) return PKV_ERR_ARG;
+  auto kern = decode_shared_prefix_kernel<T, D, BS, G>;
+  if (allow_smem<Cfg>(kern, Cfg::kSmemBytes) != PKV_OK) return PKV_ERR_CUDA;
+  dim3 grid((unsigned)p.kv_heads, (unsigned)p.num_groups, (unsigned)(p.num_parts * row_blocks));
+  kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, (int)row_blocks, maps->k, maps->v);
+  if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return launch_decode_cfg<T, D, BS, G>(p, num_seqs, part_maps, stream);
+}
+
+template <typename T>
+int launch_decode_shared(const DecodeParams& p, int num_seqs, int head_dim, int block_size,
+                         int group, int max_group_size, const DecodeMaps* maps,
+                         const DecodeMaps* part_maps, cudaStream_t stream) {
+#define PKV_SH_CASE(D_, B_, G_)                          \
+  if (head_dim == D_ && block_size == B_ && group == G_) \
+    return launch_shared_cfg<T, D_, B_, G_>(p, num_seqs, max_group_size, maps, part_maps, stream);
+#define PKV_SH_G(D_, B_) PKV_SH_CASE(D_, B_, 1) PKV_SH_CASE(D_, B_, 2) \
+  PKV_SH_CASE(D_, B_, 4) PKV_SH_CASE(D_, B_, 8)
+  PKV_SH_G(64, 8) PKV_SH_G(64, 16) PKV_SH_G(64, 32) PKV_SH_G(64, 64)
+  PKV_SH_G(128, 8) PKV_SH_G(128, 16) PKV_SH_G(128, 32) PKV_SH_G(128, 64)
+#undef PKV_SH_G
+#undef PKV_SH_CASE
+  return PKV_ERR_GEOMETRY;
 }
 
 // FP8 pools (T is the 16-bit type of q and out): the tensor-core kernel

@@ -172,6 +172,8 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
     return;
   }
   if (tok0 >= L) return;
+  // Partitions inside a shared prefix are the shared-prefix kernel's.
+  if (part < shared_parts_of(p, s)) return;
   const int ntok = min(L - tok0, PS);
   const int nparts = (L + PS - 1) / PS;
   const int nblk = (ntok + BS - 1) / BS;
