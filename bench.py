@@ -854,12 +854,16 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
         g_starts = torch.arange(0, groups * forks + 1, forks, dtype=torch.int32, device=dev)
         g_prefix = torch.full((groups,), (w.cfg["prompt"] // w.b) * w.b, dtype=torch.int32,
                               device=dev)
+        # Partitions the partition pass covers per fork after its group's
+        # shared ones: the host knows every length and prefix.
+        tail_parts = max(-(-int(L) // part) for L in w.seq_lens) - \
+            ((w.cfg["prompt"] // w.b) * w.b) // part
 
     def decode(x=resident, o=out):
         if shared:
             pkv.paged_attention_decode_shared(cache, x[0], x[4], x[5], scale, g_starts, g_prefix,
                                               forks, out=o, max_seq_len=w.max_len, workspace=ws,
-                                              partition_size=part)
+                                              partition_size=part, tail_parts=tail_parts)
         else:
             pkv.paged_attention_decode(cache, x[0], x[4], x[5], scale, out=o,
                                        max_seq_len=w.max_len, workspace=ws, partition_size=part)
@@ -1011,9 +1015,10 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
                    "kv_dtype": w.kv_dtype,
                    "kv_heads": w.Hk, "heads": w.H, "head_dim": w.D, "block_size": w.b,
                    "pool_blocks": w.N, "partition_size": part, "table": w.table_kind,
-                   "decode": ("shared prefix: %d groups of %d forks, %d positions shared"
-                              % (w.cfg["groups"], w.cfg["forks"], (w.cfg["prompt"] // w.b) * w.b)
-                              if shared else "plain"),
+                   "decode": ("shared prefix: %d groups of %d forks, %d positions shared, "
+                              "tail grid of %d partition(s)"
+                              % (w.cfg["groups"], w.cfg["forks"], (w.cfg["prompt"] // w.b) * w.b,
+                                 tail_parts) if shared else "plain"),
                    "slot_utilization": round(w.utilization, 5),
                    "l2": ("flushed before every timed step (pool %.1f MB < 2 x L2 %.0f MB)"
                           % (w.pool_bytes() / 1e6, l2_bytes / 1e6) if flush_l2 else

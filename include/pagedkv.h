@@ -80,6 +80,8 @@ typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_FP8_E4M3 = 3 } pkv_dt
 #define PKV_DEV_TIMEOUT     16u  /* a bounded wait for a bulk copy gave up        */
 #define PKV_DEV_SHARING     32u  /* shared-prefix decode: a member's table or     */
                                  /* length disagrees with its group's prefix      */
+#define PKV_DEV_LAUNCH      64u  /* a kernel found its shared memory not 1 KiB    */
+                                 /* aligned and computed nothing                  */
 /* After PKV_DEV_TIMEOUT the launch that set it may have ended with bulk
  * copies still in flight into its shared memory (the drain after a timeout
  * is itself bounded).  Treat the stream as failed: that launch's outputs,
@@ -251,8 +253,9 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
  * Same output as paged_attention_decode.  The partitions (of
  * partition_size positions) that lie wholly inside a group's shared prefix
  * are computed once per (group, KV head) for all members' queries
- * together, so each shared page is read once instead of once per member;
- * the rest of each sequence is decoded as usual and merged with them.
+ * together, on the tensor cores, so each shared page is read once instead
+ * of once per member; the rest of each sequence (its tail) is decoded by
+ * the partition pass and merged with them.
  *
  *   group_starts   device int32[num_groups + 1]: group g is the sequences
  *                  group_starts[g] .. group_starts[g+1] - 1 (consecutive,
@@ -263,6 +266,15 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
  *                  group's first member's blocks for them, and each
  *                  member's length is at least prefix.
  *   max_group_size host bound on group sizes (1 .. num_seqs).
+ *   tail_parts     host hint for the partition pass.  0: its grid spans
+ *                  every partition and the shared ones exit at once.
+ *                  n > 0: its grid spans n partitions per sequence,
+ *                  counted from the first partition after the sequence's
+ *                  group's shared ones (from partition 0 for a sequence
+ *                  outside every group); a sequence that needs more gets a
+ *                  zero output row and sets PKV_DEV_SHARING.  With forks
+ *                  whose tails fit in one partition, 1 launches one CTA per
+ *                  (sequence, KV head) instead of one per partition.
  *   workspace      as for paged_attention_decode (same size).
  *
  * A member whose table or length breaks its group's contract gets a zero
@@ -270,17 +282,17 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
  * pools; other pools decode every sequence in full (the same attention).
  * num_groups = 0 is plain decode.  Host errors as for
  * paged_attention_decode, plus PKV_ERR_ARG for num_groups outside
- * [0, 65535] or max_group_size outside [1, num_seqs], PKV_ERR_NULL /
- * PKV_ERR_ALIGN for the group arrays.
+ * [0, 65535], max_group_size outside [1, num_seqs] or tail_parts < 0,
+ * PKV_ERR_NULL / PKV_ERR_ALIGN for the group arrays.
  */
 int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
                                   const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
                                   int32_t max_seq_len, float scale, void* out,
                                   const int32_t* group_starts, const int32_t* group_prefix,
-                                  int32_t num_groups, int32_t max_group_size, void* workspace,
-                                  size_t workspace_bytes, int32_t partition_size,
-                                  cudaStream_t stream);
+                                  int32_t num_groups, int32_t max_group_size,
+                                  int32_t tail_parts, void* workspace, size_t workspace_bytes,
+                                  int32_t partition_size, cudaStream_t stream);
 
 /*
  * paged_attention_decode_static_ws -- paged_attention_decode without a

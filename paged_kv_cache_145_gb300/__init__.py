@@ -171,14 +171,16 @@ def paged_attention_decode(cache, q, block_tables, seq_lens, scale, out=None, ma
 
 def paged_attention_decode_shared(cache, q, block_tables, seq_lens, scale, group_starts,
                                   group_prefix, max_group_size, out=None, max_seq_len=0,
-                                  workspace=None, partition_size=0, stream=None):
+                                  workspace=None, partition_size=0, tail_parts=0, stream=None):
     """Decode attention like :func:`paged_attention_decode` for a batch whose
     groups of consecutive sequences share a table prefix.
 
     ``group_starts``: int32 ``[num_groups + 1]`` (group g is sequences
     ``group_starts[g] .. group_starts[g+1] - 1``); ``group_prefix``: int32
     ``[num_groups]`` positions shared by every member; ``max_group_size``:
-    host bound on group sizes.  Returns ``out``.
+    host bound on group sizes; ``tail_parts``: partitions per sequence that
+    the partition pass covers after its group's shared ones (0: all of
+    them).  Returns ``out``.
     """
     _need(q, "q", cache.io_dtype, cache.device)
     _need(block_tables, "block_tables", torch.int32, cache.device)
@@ -207,7 +209,8 @@ def paged_attention_decode_shared(cache, q, block_tables, seq_lens, scale, group
     _lib.check(_lib.lib().paged_attention_decode_shared(
         cache.ref, _ptr(q), _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), num_seqs,
         num_heads, max_seq_len, float(scale), _ptr(out), _ptr(group_starts), _ptr(group_prefix),
-        num_groups, int(max_group_size), ws_ptr, ws_len, partition_size, _stream(stream)),
+        num_groups, int(max_group_size), int(tail_parts), ws_ptr, ws_len, partition_size,
+        _stream(stream)),
         "paged_attention_decode_shared")
     return out
 

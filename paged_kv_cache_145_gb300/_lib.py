@@ -18,6 +18,7 @@ PKV_DEV_SEQ_LEN = 4
 PKV_DEV_PAIR_RANGE = 8
 PKV_DEV_TIMEOUT = 16
 PKV_DEV_SHARING = 32
+PKV_DEV_LAUNCH = 64
 
 PKV_ERR_WORKSPACE = -5
 PKV_ERR_NOMEM = -8
@@ -53,8 +54,8 @@ SIGNATURES = {
     "paged_attention_decode": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
                                               ctypes.c_float, _P, _P, ctypes.c_size_t, _I32, _P]),
     "paged_attention_decode_shared": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
-                                                     ctypes.c_float, _P, _P, _P, _I32, _I32, _P,
-                                                     ctypes.c_size_t, _I32, _P]),
+                                                     ctypes.c_float, _P, _P, _P, _I32, _I32, _I32,
+                                                     _P, ctypes.c_size_t, _I32, _P]),
     "paged_attention_decode_static_ws": (ctypes.c_int, [_CACHE, _P, _P, _I32, _P, _I32, _I32, _I32,
                                                         ctypes.c_float, _P, _I32, _P]),
     "paged_attention_prefill": (ctypes.c_int, [_CACHE, _P, _I64, _P, _I32, _I32, _P, _I32, _P,

@@ -3,7 +3,6 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
-#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -271,8 +270,8 @@ int decode_impl(const pkv_cache* cache, const void* q, const int32_t* block_tabl
                 int32_t max_blocks_per_seq, const int32_t* seq_lens, int32_t num_seqs,
                 int32_t num_heads, int32_t max_seq_len, float scale, void* out,
                 const int32_t* group_starts, const int32_t* group_prefix, int32_t num_groups,
-                int32_t max_group_size, void* workspace, size_t workspace_bytes,
-                int32_t partition_size, cudaStream_t stream) {
+                int32_t max_group_size, int32_t tail_parts, void* workspace,
+                size_t workspace_bytes, int32_t partition_size, cudaStream_t stream) {
   int rc = check_cache(cache);
   if (rc) return rc;
   rc = check_scales(cache);
@@ -336,6 +335,7 @@ int decode_impl(const pkv_cache* cache, const void* q, const int32_t* block_tabl
     p.group_starts = group_starts;
     p.group_prefix = group_prefix;
     p.num_groups = num_groups;
+    p.tail_parts = tail_parts < ws.parts ? tail_parts : 0;  // n >= the grid: the full grid
     const int D = cache->head_dim, B = cache->block_size;
     // The partition pass takes the tensor-core kernel only where the plain
     // decode would; the shared-prefix kernel always reads through the maps.
@@ -384,8 +384,8 @@ int paged_attention_decode(const pkv_cache* cache, const void* q, const int32_t*
                            void* workspace, size_t workspace_bytes, int32_t partition_size,
                            cudaStream_t stream) {
   return decode_impl(cache, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
-                     max_seq_len, scale, out, nullptr, nullptr, 0, 0, workspace, workspace_bytes,
-                     partition_size, stream);
+                     max_seq_len, scale, out, nullptr, nullptr, 0, 0, 0, workspace,
+                     workspace_bytes, partition_size, stream);
 }
 
 int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
@@ -393,11 +393,11 @@ int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
                                   const int32_t* seq_lens, int32_t num_seqs, int32_t num_heads,
                                   int32_t max_seq_len, float scale, void* out,
                                   const int32_t* group_starts, const int32_t* group_prefix,
-                                  int32_t num_groups, int32_t max_group_size, void* workspace,
-                                  size_t workspace_bytes, int32_t partition_size,
-                                  cudaStream_t stream) {
-  if (num_groups < 0 || num_groups > 65535 || (num_groups > 0 && (max_group_size < 1 ||
-                                                                  max_group_size > num_seqs)))
+                                  int32_t num_groups, int32_t max_group_size,
+                                  int32_t tail_parts, void* workspace, size_t workspace_bytes,
+                                  int32_t partition_size, cudaStream_t stream) {
+  if (num_groups < 0 || num_groups > 65535 || tail_parts < 0 ||
+      (num_groups > 0 && (max_group_size < 1 || max_group_size > num_seqs)))
     return PKV_ERR_ARG;
   if (num_groups > 0 && (!group_starts || !group_prefix)) return PKV_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(group_starts) & 3u) ||
@@ -405,7 +405,8 @@ int paged_attention_decode_shared(const pkv_cache* cache, const void* q,
     return PKV_ERR_ALIGN;
   return decode_impl(cache, q, block_tables, max_blocks_per_seq, seq_lens, num_seqs, num_heads,
                      max_seq_len, scale, out, group_starts, group_prefix, num_groups,
-                     max_group_size, workspace, workspace_bytes, partition_size, stream);
+                     max_group_size, tail_parts, workspace, workspace_bytes, partition_size,
+                     stream);
 }
 
 int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total_queries,

@@ -80,30 +80,59 @@ struct DecodeParams {
   const int32_t* group_prefix;
   int num_groups;
   int num_seqs;
+  // Partition pass of the shared-prefix decode: 0, slice z is partition z
+  // (the shared ones exit); tail_parts > 0, the grid has tail_parts slices
+  // and slice z is the z-th partition after the sequence's shared ones.
+  int tail_parts;
 };
 
-// Group owning sequence s, or -1: the last g with group_starts[g] <= s,
-// provided s < group_starts[g+1].  The shared-prefix kernel and the
-// partition pass both use this rule, so a malformed group list can leave a
-// sequence without a group (decoded plainly) but never covered twice.
+// Group owning sequence s, or -1: the last g with group_starts[g] <= s
+// (for a nondecreasing list, the group whose range holds s), provided
+// s < group_starts[g+1].  The search is 32-way: each round issues its
+// probes together, so a list of up to 32 groups costs one round of loads
+// (a binary search would cost one dependent load per halving, and every
+// CTA of the partition pass asks).  It is a fixed function of the list, and
+// the shared-prefix kernel and the partition pass both call it, so a
+// malformed list can leave a sequence without a group (decoded plainly) but
+// never covered twice.
 __device__ __forceinline__ int shared_owner(const DecodeParams& p, int s) {
   if (!p.group_starts || p.num_groups <= 0) return -1;
-  int lo = 0, hi = p.num_groups - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (ld_nc(p.group_starts + mid) <= s) lo = mid;
-    else hi = mid - 1;
+  const int32_t* gs = p.group_starts;
+  int lo = 0, cnt = p.num_groups;  // candidates lo .. lo + cnt - 1; lo + cnt <= num_groups
+  while (cnt > 32) {
+    const int step = (cnt + 31) / 32;
+    int best = 0;
+#pragma unroll
+    for (int i = 1; i < 32; ++i) {
+      const int off = i * step;
+      if (off < cnt && ld_nc(gs + lo + off) <= s) best = i;
+    }
+    lo += best * step;
+    cnt = min(step, cnt - best * step);
   }
-  const int a = ld_nc(p.group_starts + lo), b = ld_nc(p.group_starts + lo + 1);
-  return (a <= s && s < b) ? lo : -1;
+  // Last round: entries lo .. lo + cnt (each candidate's start and the end
+  // of the last one).
+  int v[33];
+#pragma unroll
+  for (int i = 0; i < 33; ++i) v[i] = i <= cnt ? ld_nc(gs + lo + i) : 0;
+  int a = v[0], b = v[1], g = 0;
+#pragma unroll
+  for (int i = 1; i < 32; ++i)
+    if (i < cnt && v[i] <= s) {
+      g = i;
+      a = v[i];
+      b = v[i + 1];
+    }
+  return (a <= s && s < b) ? lo + g : -1;
 }
 
-// Partitions of sequence s that the shared-prefix kernel computes.
+// Partitions of sequence s that the shared-prefix kernel computes (at most
+// the grid's partitions).
 __device__ __forceinline__ int shared_parts_of(const DecodeParams& p, int s) {
   const int g = shared_owner(p, s);
   if (g < 0) return 0;
   const int pre = ld_nc(p.group_prefix + g);
-  return pre > 0 ? pre / p.part_size : 0;
+  return pre > 0 ? min(pre / p.part_size, p.num_parts) : 0;
 }
 
 constexpr int kMaxPartSize = 8192;
@@ -185,26 +214,32 @@ decode_partition_kernel(const DecodeParams p) {
   // past a sequence's end (which exit at once) gather at the end of the grid.
   const int kvh = blockIdx.x;
   const int s = blockIdx.y;
-  const int part = blockIdx.z;
+  const int z = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int H = p.num_heads;
   T* out = static_cast<T*>(p.out);
   const int64_t out0 = ((int64_t)s * H + (int64_t)kvh * G) * D;  // out[s][kvh*G][0]
   const int PS = p.part_size;
+  // The length, and with a tail grid (tail_parts > 0: slice z is the z-th
+  // partition after the sequence's shared ones) the sequence's group, are
+  // loaded first; otherwise slice z is partition z, and the length and this
+  // partition's table entries are loaded together (the entries
+  // speculatively, but never past the table row), so a CTA waits for one
+  // global round trip before it can issue its first bulk copy.
+  const int L = ld_nc(p.seq_lens + s);
+  const bool tail_grid = p.tail_parts > 0;
+  int shared_parts = tail_grid ? shared_parts_of(p, s) : 0;
+  const int part = z + shared_parts;
   const int tok0 = part * PS;
   const int blk0 = tok0 / BS;
-
-  // The length and this partition's table entries are loaded together (the
-  // entries speculatively, but never past the table row), so a CTA waits
-  // for one global round trip before it can issue its first bulk copy.
   const int32_t* trow = p.tables + (int64_t)s * p.max_blocks + blk0;
   const int span = min(PS / BS, p.max_blocks - blk0);
-  const int L = ld_nc(p.seq_lens + s);
   const int e_first = (int)threadIdx.x < span ? ld_nc(trow + threadIdx.x) : -1;
+  if (!tail_grid) shared_parts = shared_parts_of(p, s);  // loads issued with the two above
 
   if (L < 1 || L > p.max_len) {
-    if (part == 0) {
+    if (z == 0) {
       for (int e = threadIdx.x; e < G * D; e += Cfg::kThreads) out[out0 + e] = Elem<T>::from_f(0.f);
       if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SEQ_LEN);
     }
@@ -212,9 +247,17 @@ decode_partition_kernel(const DecodeParams p) {
   }
   if (tok0 >= L) return;
   // Partitions inside a shared prefix are the shared-prefix kernel's.
-  if (part < shared_parts_of(p, s)) return;
+  if (part < shared_parts) return;
   const int ntok = min(L - tok0, PS);
   const int nparts = (L + PS - 1) / PS;
+  if (tail_grid && z == p.tail_parts - 1 && part + 1 < nparts) {
+    // The sequence needs partitions past the tail grid: their slots get the
+    // invalid marker (nobody else writes them), so the merge zeroes its rows.
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SHARING);
+    for (int i = threadIdx.x; i < G * (nparts - part - 1); i += Cfg::kThreads)
+      p.ws_ml[((int64_t)s * H + (int64_t)kvh * G + i % G) * p.num_parts + part + 1 + i / G] =
+          make_float2(-INFINITY, -1.f);
+  }
   const int nblk = (ntok + BS - 1) / BS;
   const int nchunks = (ntok + C - 1) / C;
 

@@ -57,10 +57,13 @@ void launch_reduce(const DecodeParams& p, int num_seqs, cudaStream_t stream) {
 template <typename T, int D, int BS, int G>
 int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* maps,
                       cudaStream_t stream) {
-  dim3 grid((unsigned)p.kv_heads, (unsigned)num_seqs, (unsigned)p.num_parts);
+  dim3 grid((unsigned)p.kv_heads, (unsigned)num_seqs,
+            (unsigned)(p.tail_parts > 0 ? p.tail_parts : p.num_parts));
   bool launched = false;
   if constexpr (mma_eligible<T, D, BS, G>()) {
-    if (maps) {
+    // A one-slice tail grid (short tails, one CTA per sequence and KV head)
+    // runs on the CUDA-core kernel: more of its CTAs fit on an SM.
+    if (maps && p.tail_parts != 1) {
       using Cfg = MmaCfg<T, D, BS, G>;
       auto kern = decode_partition_mma_kernel<T, D, BS, G>;
       if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
@@ -82,17 +85,29 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* map
 // the partition pass over the rest and the merge.
 // `maps` feed the shared-prefix kernel; `part_maps` (null: CUDA-core
 // kernel) the partition pass, as in the plain decode.
-template <typename T, int D, int BS, int G>
-int launch_shared_cfg(const DecodeParams& p, int num_seqs, int max_group_size,
-                      const DecodeMaps* maps, const DecodeMaps* part_maps, cudaStream_t stream) {
-  using Cfg = SharedCfg<T, D, BS, G>;
+template <typename T, int D, int BS, int G, int DUP>
+int launch_shared_dup(const DecodeParams& p, int max_group_size, const DecodeMaps* maps,
+                      cudaStream_t stream) {
+  using Cfg = SharedTcCfg<T, D, BS, G, DUP>;
   const int64_t row_blocks = ((int64_t)max_group_size * G + Cfg::kRows - 1) / Cfg::kRows;
   if ((int64_t)p.num_parts * row_blocks > 65535) return PKV_ERR_ARG;
-  auto kern = decode_shared_prefix_kernel<T, D, BS, G>;
+  auto kern = decode_shared_prefix_kernel<T, D, BS, G, DUP>;
   if (allow_smem<Cfg>(kern, Cfg::kSmemBytes) != PKV_OK) return PKV_ERR_CUDA;
   dim3 grid((unsigned)p.kv_heads, (unsigned)p.num_groups, (unsigned)(p.num_parts * row_blocks));
   kern<<<grid, Cfg::kThreads, Cfg::kSmemBytes, stream>>>(p, (int)row_blocks, maps->k, maps->v);
-  if (cudaPeekAtLastError() != cudaSuccess) return PKV_ERR_CUDA;
+  return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+// Groups of at most 32 stacked rows (max_group_size x G) run with every row
+// four times over the MMA's 128 rows, the copies splitting the softmax
+// work; larger groups in blocks of 128 rows.
+template <typename T, int D, int BS, int G>
+int launch_shared_cfg(const DecodeParams& p, int num_seqs, int max_group_size,
+                      const DecodeMaps* maps, const DecodeMaps* part_maps, cudaStream_t stream) {
+  const int rc = (int64_t)max_group_size * G <= 32
+                     ? launch_shared_dup<T, D, BS, G, 4>(p, max_group_size, maps, stream)
+                     : launch_shared_dup<T, D, BS, G, 1>(p, max_group_size, maps, stream);
+  if (rc != PKV_OK) return rc;
   return launch_decode_cfg<T, D, BS, G>(p, num_seqs, part_maps, stream);
 }
 

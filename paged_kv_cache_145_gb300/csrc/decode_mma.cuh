@@ -147,7 +147,7 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
 
   const int kvh = blockIdx.x;
   const int s = blockIdx.y;
-  const int part = blockIdx.z;
+  const int z = blockIdx.z;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int gi = lane >> 2;  // fragment row group (position, or head for B)
@@ -156,16 +156,25 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
   T* out = static_cast<T*>(p.out);
   const int64_t out0 = ((int64_t)s * H + (int64_t)kvh * G) * D;
   const int PS = p.part_size;
+  // The length, and with a tail grid (tail_parts > 0: slice z is the z-th
+  // partition after the sequence's shared ones) the sequence's group, are
+  // loaded first; otherwise slice z is partition z, and the length and this
+  // partition's table entries are loaded together (the entries
+  // speculatively, but never past the table row), so a CTA waits for one
+  // global round trip before it can issue its first bulk copy.
+  const int L = ld_nc(p.seq_lens + s);
+  const bool tail_grid = p.tail_parts > 0;
+  int shared_parts = tail_grid ? shared_parts_of(p, s) : 0;
+  const int part = z + shared_parts;
   const int tok0 = part * PS;
   const int blk0 = tok0 / BS;
-
   const int32_t* trow = p.tables + (int64_t)s * p.max_blocks + blk0;
   const int span = min(PS / BS, p.max_blocks - blk0);
-  const int L = ld_nc(p.seq_lens + s);
   const int e_first = (int)threadIdx.x < span ? ld_nc(trow + threadIdx.x) : -1;
+  if (!tail_grid) shared_parts = shared_parts_of(p, s);  // loads issued with the two above
 
   if (L < 1 || L > p.max_len) {
-    if (part == 0) {
+    if (z == 0) {
       for (int e = threadIdx.x; e < G * D; e += Cfg::kThreads) out[out0 + e] = Elem<T>::from_f(0.f);
       if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SEQ_LEN);
     }
@@ -173,9 +182,17 @@ decode_partition_mma_kernel(const DecodeParams p, const __grid_constant__ CUtens
   }
   if (tok0 >= L) return;
   // Partitions inside a shared prefix are the shared-prefix kernel's.
-  if (part < shared_parts_of(p, s)) return;
+  if (part < shared_parts) return;
   const int ntok = min(L - tok0, PS);
   const int nparts = (L + PS - 1) / PS;
+  if (tail_grid && z == p.tail_parts - 1 && part + 1 < nparts) {
+    // The sequence needs partitions past the tail grid: their slots get the
+    // invalid marker (nobody else writes them), so the merge zeroes its rows.
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SHARING);
+    for (int i = threadIdx.x; i < G * (nparts - part - 1); i += Cfg::kThreads)
+      p.ws_ml[((int64_t)s * H + (int64_t)kvh * G + i % G) * p.num_parts + part + 1 + i / G] =
+          make_float2(-INFINITY, -1.f);
+  }
   const int nblk = (ntok + BS - 1) / BS;
   const int nchunks = (ntok + C - 1) / C;
 

@@ -18,19 +18,46 @@
 // those partitions, and the split-K merge combines them with the member's
 // own tail unchanged.
 //
-// Kernel (this library's design): grid (KV head, group, shared partition x
-// row block); one producer warp streams the partition's 16-position K/V
-// chunks through a four-stage ring of TMA tile loads (128-byte swizzle),
-// read through the first member's table; four compute warps each own 8 of
-// the group's stacked rows (member r / G, query head r % G) and run every
-// chunk with the grouped-head kernel's per-chunk steps (S^T = K.Q^T and
-// O^T += V^T.P^T as mma.sync m16n8k16 tiles, online softmax per column,
-// bf16 P in two parts).  Each warp writes its rows' partials directly; no
-// cross-warp merge is needed.
+// Kernel (this library's design), on the fifth-generation tensor cores:
+// grid (KV head, group, shared partition x row block).  The 128 rows of
+// the MMAs (tensor-memory lanes) hold a row block's stacked rows (member
+// r / G, query head r % G), each DUP times: 128 rows once, or, for groups
+// of at most 32 stacked rows, every row four times, so that the four
+// copies split each key tile's softmax work between them.  Keys stream in
+// tiles of 64 positions, read through the group's first member's table.
+// Six warps:
+//   warps 0-3  softmax: thread = one copy of a row, lane = tensor-memory
+//              lane: loads its S row, takes its 64 / DUP keys of it, keeps
+//              the running maximum (shared by the copies; raised lazily,
+//              only when a tile's maximum exceeds it by more than 2^8) and
+//              its part of the sum, writes P for its keys (zeros for the
+//              others) into its columns, rescales its O row when the
+//              maximum moves; at the end the copies' O rows and sums add up
+//              to the row's, which the copies write together; warps with no
+//              real row idle;
+//   warp 4     producer: 4-D TMA tile loads (128-byte swizzle) of key and
+//              value tiles into two rings (values stay longer: three stages
+//              against two for keys), reading the table one tile ahead;
+//              allocates the tensor memory;
+//   warp 5     MMA issuer (one thread): S = Q.K^T (A = the stacked query
+//              rows, B = the key tile, both K-major in shared memory, 128 x
+//              64 x D), and O += P.V (A = P in tensor memory, B = the value
+//              tile as copied, read MN-major, 128 x D x 64).  bf16 pools
+//              take P in two bf16 parts, the truncated weight and its
+//              rounded remainder (about 16 bits of P); fp16 pools one fp16
+//              part.  S of the next tile is issued while the softmax works
+//              on the current one.
+// Tensor memory (256 columns): S at 0 (64), P at 64 (64: keys 2c, 2c+1 in
+// column c, a low part in 32 + c), O at 128 (D).  Shared memory: barriers
+// and flags in the first KiB, then the query rows and the two rings, 1 KiB
+// aligned (the dynamic base must be, else the kernel flags PKV_DEV_LAUNCH
+// and computes nothing); two CTAs fit on an SM and a third does not, so
+// their tensor-memory allocations always fit.  Every wait is bounded; on a
+// timeout the roles stop, the issuer waits for its MMAs, the producer for
+// its copies, and the tensor memory is released.
 //
-// Ownership.  Sequence s belongs to group owner(s): the last g with
-// group_starts[g] <= s, provided s < group_starts[g+1]; both this kernel and
-// the partition pass use that rule, so a malformed list can only leave
+// Ownership.  Sequence s belongs to group shared_owner(s); this kernel and
+// the partition pass both use that rule, so a malformed list can only leave
 // sequences without a group (decoded plainly), never covered twice or not
 // at all.  Checked per row: the length lies in [1, max_len] (else the row is
 // left to the plain path's invalid-length handling), covers the partition,
@@ -39,48 +66,77 @@
 // set.
 #pragma once
 
+#include <type_traits>
+
 #include "decode_mma.cuh"
+#include "tcgen05.cuh"
 
 namespace pkv {
 
-template <typename T, int D, int BS, int G>
-struct SharedCfg {
-  static constexpr int kComputeWarps = 4;
-  static constexpr int kRowsPerWarp = 8;                 // n of m16n8k16: query rows
-  static constexpr int kRows = kComputeWarps * kRowsPerWarp;
-  static constexpr int kThreads = (kComputeWarps + 1) * 32;  // + producer warp
-  static constexpr int kChunk = 16;
+template <typename T, int D, int BS, int G, int DUP>
+struct SharedTcCfg {
+  static constexpr int kLanes = 128;                       // MMA rows = tensor-memory lanes
+  static constexpr int kDup = DUP;                         // copies of each stacked row
+  static constexpr int kRowsPerWarp = 32 / DUP;            // stacked rows per softmax warp
+  static constexpr int kRows = 4 * kRowsPerWarp;           // stacked rows per CTA
+  static constexpr int kKeysPerCopy = 64 / DUP;
+  static constexpr int kDimsPerCopy = 32 / DUP;            // of each 32-dim chunk of O
+  static constexpr int kKeys = 64;                         // positions per K/V tile
+  static constexpr int kHalves = D / 64;                   // 128-byte column blocks of a row
+  static constexpr int kQHalfBytes = kLanes * 128;
+  static constexpr int kQBytes = kHalves * kQHalfBytes;    // the stacked query rows
+  static constexpr int kKvHalfBytes = kKeys * 128;
+  static constexpr int kKvBytes = kHalves * kKvHalfBytes;  // one key (or value) tile
+  static constexpr int kKStages = D == 64 ? 4 : 2;
+  static constexpr int kVStages = D == 64 ? 6 : 3;
   static constexpr int kBoxRows = BS < 16 ? BS : 16;
-  static constexpr int kBoxesPerChunk = kChunk / kBoxRows;
-  static constexpr int kCols = D / 64;                   // 128-byte column boxes per row
-  static constexpr int kBoxBytes = kChunk * 128;
-  static constexpr int kTileBytes = kCols * kBoxBytes;   // one chunk of K (or V)
-  static constexpr int kStageBytes = 2 * kTileBytes;
-  static constexpr int kStages = 4;
-  static constexpr int kBarOff = kStages * kStageBytes;
-  static constexpr int kPtOff = kBarOff + 2 * kStages * 8;
-  static constexpr int kPtBytes = 2 * 8 * kChunk * 2;    // P^T high and low parts
-  static constexpr int kTableOff = kPtOff + kComputeWarps * kPtBytes;
-  static constexpr int kAlign = 1024;
-  static constexpr int kSmemBytes = kAlign + kTableOff + (kMaxPartSize / BS) * 4;
-  static_assert((BS % kChunk == 0 || kChunk % BS == 0) && D % 64 == 0 && G <= 8, "geometry");
+  static constexpr int kBoxes = kKeys / kBoxRows;          // TMA boxes per tile per column block
+  static constexpr int kProducerWarp = 4;
+  static constexpr int kMmaWarp = 5;
+  static constexpr int kThreads = 6 * 32;
+  // First KiB: barriers, the tensor-memory slot, per-member flags.
+  static constexpr int kNumBars = 2 * kKStages + 2 * kVStages + 6;
+  static constexpr int kBarOff = 0;
+  static constexpr int kSlotOff = 256;
+  static constexpr int kMemberOff = 512;                   // per member of the row block: mismatch
+  static constexpr int kQOff = 1024;
+  static constexpr int kKRingOff = kQOff + kQBytes;
+  static constexpr int kVRingOff = kKRingOff + kKStages * kKvBytes;
+  static constexpr int kSmemBytes = kVRingOff + kVStages * kKvBytes;
+  static constexpr uint32_t kTmemCols = 256;
+  static constexpr uint32_t kSCol = 0, kPCol = 64, kOCol = 128;
+  static constexpr bool kTwoPartP = std::is_same<T, __nv_bfloat16>::value;
+  static constexpr uint32_t kFmt = kTwoPartP ? 1u : 0u;
+  static constexpr uint32_t kIdescS = idesc_f16(kFmt, 128, kKeys, false);
+  static constexpr uint32_t kIdescPV = idesc_f16(kFmt, 128, D, true);
+  // An SM holds 228 KiB of shared memory, 1 KiB of it reserved per CTA.
+  static_assert(2 * (kSmemBytes + 1024) <= 228 * 1024, "two CTAs per SM");
+  static_assert(3 * (kSmemBytes + 1024) > 228 * 1024, "not three (tensor memory)");
+  static_assert(kNumBars * 8 <= kSlotOff && kMemberOff + kRows * 4 <= kQOff, "header");
+  static_assert(kOCol + D <= kTmemCols, "tensor memory");
+  static_assert(kQBytes % 1024 == 0 && kKvBytes % 1024 == 0, "128-byte swizzle atoms");
+  static_assert(kBoxes <= 32 && D % 64 == 0 && G <= 8, "geometry");
+  static_assert(DUP == 1 || DUP == 2 || DUP == 4, "copies of a row: adjacent lanes");
 };
 
-template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(SharedCfg<T, D, BS, G>::kThreads)
+template <typename T, int D, int BS, int G, int DUP>
+__global__ void __launch_bounds__(SharedTcCfg<T, D, BS, G, DUP>::kThreads)
 decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
                             const __grid_constant__ CUtensorMap tmk,
                             const __grid_constant__ CUtensorMap tmv) {
-  using Cfg = SharedCfg<T, D, BS, G>;
-  using Op = MmaOp<T>;
-  constexpr int C = Cfg::kChunk;
-  constexpr int NW = Cfg::kComputeWarps;
-  constexpr int NST = Cfg::kStages;
-  constexpr int KSTEPS = D / 16;
-  constexpr bool kSplitP = std::is_same<T, __nv_bfloat16>::value;
-  extern __shared__ __align__(128) unsigned char smem_raw[];
-  unsigned char* smem = smem_raw + ((Cfg::kAlign - (smem_addr(smem_raw) & (Cfg::kAlign - 1))) &
-                                    (Cfg::kAlign - 1));
+  using Cfg = SharedTcCfg<T, D, BS, G, DUP>;
+  constexpr int NK = Cfg::kKStages;
+  constexpr int NV = Cfg::kVStages;
+  constexpr int KT = Cfg::kKeys;
+  constexpr int KW = Cfg::kKeysPerCopy;
+  constexpr int DW = Cfg::kDimsPerCopy;
+  constexpr int RB = Cfg::kBoxRows;
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t sbase = smem_addr(smem);
+  if (sbase & 1023u) {  // the swizzled tiles need a 1 KiB aligned base
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_LAUNCH);
+    return;
+  }
 
   const int kvh = blockIdx.x;
   const int g = blockIdx.y;
@@ -97,250 +153,468 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
   const int pre = ld_nc(p.group_prefix + g);
   if (s0 < 0 || s1 <= s0 || pre < PS || part >= pre / PS) return;
   const int gsize = s1 - s0;
-  if (rb * Cfg::kRows >= gsize * G) return;
+  const int row0 = rb * Cfg::kRows;  // first stacked row of this CTA
+  const int nrows = min(Cfg::kRows, gsize * G - row0);
+  if (nrows <= 0) return;
   const int tok0 = part * PS;
   const int blk0 = tok0 / BS;
-  const int span = PS / BS;  // blocks of the partition (<= max_blocks - blk0: checked below)
-  const int nchunks = (PS + C - 1) / C;
-
-  // ---- the leader's table entries for this partition ------------------------
-  int* stable = reinterpret_cast<int*>(smem + Cfg::kTableOff);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
-  uint64_t* empty = full + NST;
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < NST; ++st) {
-      mbar_init(smem_addr(&full[st]), 1);
-      mbar_init(smem_addr(&empty[st]), NW);
-    }
-    fence_mbar_init();
-  }
+  const int span = PS / BS;  // blocks of the partition
+  const int n_tiles = (PS + KT - 1) / KT;
   const bool fits = blk0 + span <= p.max_blocks;
   const int32_t* lrow = p.tables + (int64_t)s0 * p.max_blocks + blk0;
+  const int m_first = row0 / G;  // first member with a row here
+
+  int* member_bad = reinterpret_cast<int*>(smem + Cfg::kMemberOff);
+  const uint32_t bar0 = sbase + Cfg::kBarOff;
+  auto k_full = [&](int st) { return bar0 + 8u * st; };
+  auto k_empty = [&](int st) { return bar0 + 8u * (NK + st); };
+  auto v_full = [&](int st) { return bar0 + 8u * (2 * NK + st); };
+  auto v_empty = [&](int st) { return bar0 + 8u * (2 * NK + NV + st); };
+  const uint32_t s_full = bar0 + 8u * (2 * NK + 2 * NV);  // S written
+  const uint32_t s_free = s_full + 8;                      // S read by every softmax thread
+  const uint32_t p_full = s_full + 16;                     // P written (and O rescaled)
+  const uint32_t p_free = s_full + 24;                     // P.V done
+  const uint32_t o_last = s_full + 32;                     // the last P.V done (single use)
+  const uint32_t drain = s_full + 40;                      // every MMA done (single use)
+  const int nsw = (nrows + Cfg::kRowsPerWarp - 1) / Cfg::kRowsPerWarp;  // warps with real rows
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < NK; ++st) {
+      mbar_init(k_full(st), 1);
+      mbar_init(k_empty(st), 1);
+    }
+    for (int st = 0; st < NV; ++st) {
+      mbar_init(v_full(st), 1);
+      mbar_init(v_empty(st), 1);
+    }
+    mbar_init(s_full, 1);
+    mbar_init(s_free, nsw * 32);
+    mbar_init(p_full, nsw * 32);
+    mbar_init(p_free, 1);
+    mbar_init(o_last, 1);
+    mbar_init(drain, 1);
+    fence_mbar_init();
+  }
+  for (int i = threadIdx.x; i < Cfg::kRows; i += Cfg::kThreads) member_bad[i] = 0;
+  __syncthreads();
+
+  // ---- rows: lane `lane` of softmax warp `warp` (tensor-memory lane
+  // 32 warp + lane) is copy `cp` of stacked row R = row0 + r_local.  Loads
+  // issued together: its length, its group (shared_owner), its member's
+  // table entries for the partition against the leader's (the member's
+  // threads in this CTA split them), the leader's entries (range check, all
+  // threads), and the query row.  Status: 1 usable, 0 skip (not owned, or
+  // an invalid length: the plain path zeroes it), -1 sharing contract
+  // broken.
+  const int cp = lane % DUP;
+  const int r_local = warp * Cfg::kRowsPerWarp + lane / DUP;
+  const int R = row0 + r_local;
+  const bool has_row = warp < 4 && r_local < nrows;
+  const int head = kvh * G + R % G;
+  int my_seq = -1, my_status = 0, my_len = 0;
+  uint4 qv[D / 8];
+  if (has_row) {
+    const int mi = R / G;
+    const int s = s0 + mi;
+    const uint4* qrow =
+        reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + ((int64_t)s * H + head) * D);
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qv[c] = qrow[c];
+    const int L = ld_nc(p.seq_lens + s);
+    const int own = shared_owner(p, s);
+    if (fits) {
+      const int r_lo = max(row0, mi * G), r_hi = min(row0 + nrows, (mi + 1) * G);
+      const int32_t* row = p.tables + (int64_t)s * p.max_blocks + blk0;
+      int mismatch = 0;
+#pragma unroll 4
+      for (int i = (R - r_lo) * DUP + cp; i < span; i += (r_hi - r_lo) * DUP)
+        mismatch |= ld_nc(row + i) != ld_nc(lrow + i);
+      if (mismatch) atomicOr(member_bad + (mi - m_first), 1);
+    }
+    if (own == g) {
+      my_seq = s;
+      my_len = L;
+      my_status = (L < 1 || L > p.max_len) ? 0 : 1;
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) qv[c] = make_uint4(0u, 0u, 0u, 0u);
+  }
   int bad = !fits;
   for (int i = threadIdx.x; fits && i < span; i += Cfg::kThreads) {
     const int e = ld_nc(lrow + i);
     bad |= (e < 0 || (int64_t)e >= p.num_blocks);
-    stable[i] = e;
   }
-  // The leader's entries are unusable: every member's row of this partition
-  // is marked invalid below.
+  // The leader's entries are unusable: every member's row is marked invalid.
   bad = __syncthreads_or(bad);
+  if (has_row && my_status == 1 &&
+      (bad || my_len < tok0 + PS || member_bad[R / G - m_first] != 0))
+    my_status = -1;
 
-  // ---- this thread's row (compute warps): lanes' B-fragment column gi -----
-  const int gi = lane >> 2, ti = lane & 3;
-  auto row_seq = [&](int col) {  // sequence of column col of this warp, or -1
-    const int r = rb * Cfg::kRows + warp * 8 + col;
-    const int m = r / G;
-    if (warp >= NW || m >= gsize) return -1;
-    const int s = s0 + m;
-    return shared_owner(p, s) == g ? s : -1;
-  };
-  // Row status per column: 1 usable, 0 skip (invalid length: the plain
-  // path zeroes it), -1 sharing contract broken (marked invalid).
-  auto row_status = [&](int s) -> int {
-    if (s < 0) return 0;
-    const int L = ld_nc(p.seq_lens + s);
-    if (L < 1 || L > p.max_len) return 0;
-    if (bad || L < tok0 + PS) return -1;
-    const int32_t* row = p.tables + (int64_t)s * p.max_blocks + blk0;
-    for (int i = 0; i < span; ++i)
-      if (ld_nc(row + i) != stable[i]) return -1;
-    return 1;
-  };
-
-  if (warp == NW) {
-    // ---- producer: chunk c = positions 16c .. 16c+15 of the partition ------
-    const uint64_t policy = policy_evict_first();
-    const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
-    bool ok = !bad;
-    int issued = 0;
-    for (int j = 0; j < nchunks && ok; ++j) {
-      const int st = j % NST;
-      if (j >= NST)
-        ok = !__any_sync(kFullMask,
-                         !mbar_wait(smem_addr(&empty[st]), (uint32_t)(((j / NST) - 1) & 1)));
-      if (!ok) break;
-      if (lane == 0) {
-        const uint32_t bar = smem_addr(&full[st]);
-        const uint32_t dst = smem_addr(smem) + st * Cfg::kStageBytes;
-        constexpr int RB = Cfg::kBoxRows;
-        mbar_arrive_expect_tx(bar, Cfg::kStageBytes);
-        for (int hb = 0; hb < Cfg::kBoxesPerChunk; ++hb) {
-          // A box past the partition's end (b = 8, odd number of blocks)
-          // reads an out-of-range block: the copy fills it with zeros.
-          const int pos = j * C + hb * RB;
-          const int pb = pos < PS ? stable[pos / BS] : oob_block;
-          const int row = pos < PS ? pos % BS : 0;
+  // ---- this copy's DW dims of a row's partial, from dim d0 (v: the row's
+  //      sums): o = O / l with (m, l), or the invalid marker ----------------
+  auto store_row = [&](bool broken, float m, float l, const uint32_t(&v)[DW], int d0) {
+    const int nparts = (my_len + PS - 1) / PS;
+    const float inv = broken ? 0.f : 1.f / l;
+    auto f = [&](int d) { return broken ? 0.f : __uint_as_float(v[d]) * inv; };
+    if (nparts == 1) {  // the whole sequence is this partition: final output
+      uint4* orow = reinterpret_cast<uint4*>(out + ((int64_t)my_seq * H + head) * D + d0);
 #pragma unroll
-          for (int cb = 0; cb < Cfg::kCols; ++cb) {
-            const uint32_t o = cb * Cfg::kBoxBytes + hb * RB * 128;
-            tma_load_4d(dst + o, &tmk, cb * 64, row, kvh, pb, bar, policy);
-            tma_load_4d(dst + Cfg::kTileBytes + o, &tmv, cb * 64, row, kvh, pb, bar, policy);
-          }
-        }
+      for (int u = 0; u < DW / 8; ++u) {
+        uint4 w;
+        w.x = pack_pair<T>(f(8 * u + 0), f(8 * u + 1));
+        w.y = pack_pair<T>(f(8 * u + 2), f(8 * u + 3));
+        w.z = pack_pair<T>(f(8 * u + 4), f(8 * u + 5));
+        w.w = pack_pair<T>(f(8 * u + 6), f(8 * u + 7));
+        orow[u] = w;
       }
-      __syncwarp();
-      issued = j + 1;
+    } else {
+      const int64_t w = ((int64_t)my_seq * H + head) * p.num_parts + part;
+      float4* orow = reinterpret_cast<float4*>(p.ws_o + w * D + d0);
+#pragma unroll
+      for (int u = 0; u < DW / 4; ++u)
+        orow[u] = make_float4(f(4 * u), f(4 * u + 1), f(4 * u + 2), f(4 * u + 3));
+      if (d0 == 0) p.ws_ml[w] = broken ? make_float2(-INFINITY, -1.f) : make_float2(m, l);
     }
-    // Copies issued but possibly never consumed (a compute warp stopped).
-    for (int j = issued - NST < 0 ? 0 : issued - NST; j < issued; ++j)
-      mbar_wait(smem_addr(&full[j % NST]), (uint32_t)((j / NST) & 1), kWaitLimitNs / 8);
-    if (!ok && !bad && lane == 0) set_error(p.err, PKV_DEV_TIMEOUT);
+  };
+  // Rows whose partial is the invalid marker: status -1, and with `all`
+  // (nothing computed, or a wait gave up) every usable row too.
+  auto mark_broken_rows = [&](bool all) {
+    if (!has_row || my_status == 0 || (!all && my_status == 1)) return;
+    if (my_status < 0 && cp == 0) set_error(p.err, PKV_DEV_SHARING);
+    const uint32_t zero[DW] = {};
+    for (int c0 = 0; c0 < D; c0 += 32) store_row(true, 0.f, 0.f, zero, c0 + cp * DW);
+  };
+  if (bad) {  // no tensor-core work: every usable row is now broken
+    mark_broken_rows(true);
     return;
   }
 
-  // ---- compute warps ---------------------------------------------------------
-  // Column gi (B fragments): the query row this lane loads; columns 2ti and
-  // 2ti+1 (accumulators): the rows this lane's results belong to.
-  const int sq = row_seq(gi);
-  const int hq = kvh * G + (rb * Cfg::kRows + warp * 8 + gi) % G;
-  uint32_t qb[KSTEPS][2];
-  {
-    const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-        static_cast<const T*>(p.q) + ((int64_t)(sq < 0 ? 0 : sq) * H + hq) * D);
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      qb[kk][0] = sq >= 0 ? qrow[(16 * kk + 2 * ti) / 2] : 0u;
-      qb[kk][1] = sq >= 0 ? qrow[(16 * kk + 2 * ti + 8) / 2] : 0u;
-    }
+  // ---- tensor memory; the stacked query rows (zeros where unusable) --------
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Cfg::kSlotOff);
+  if (warp == Cfg::kProducerWarp) {
+    tmem_alloc(smem_addr(slot), Cfg::kTmemCols);
+    tmem_relinquish();
   }
-  float acc[KSTEPS][4];
+  if (warp < 4) {
+    const bool use = has_row && my_status == 1;
+    const int qr = warp * 32 + lane;  // this thread's MMA row
 #pragma unroll
-  for (int i = 0; i < KSTEPS; ++i)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[i][c] = 0.f;
-  float m[2] = {-INFINITY, -INFINITY};
-  float l[2] = {0.f, 0.f};
-  bool timed_out = false;
-
-  const int mm = lane >> 3, mr = lane & 7;
-  const int k_tok = (mm & 1) * 8 + mr, k_col8 = mm >> 1;
-  const int v_tok = (mm >> 1) * 8 + mr, v_col8 = mm & 1;
-  uint16_t* pt = reinterpret_cast<uint16_t*>(smem + Cfg::kPtOff + warp * Cfg::kPtBytes);
-  const uint32_t ring0 = smem_addr(smem);
-
-  for (int j = 0; j < nchunks && !bad; ++j) {
-    const int st = j % NST;
-    timed_out = __any_sync(kFullMask, !mbar_wait(smem_addr(&full[st]), (uint32_t)((j / NST) & 1)));
-    if (timed_out) break;
-    const int nvalid = min(C, PS - j * C);
-    const uint32_t ktile = ring0 + st * Cfg::kStageBytes;
-    const uint32_t vtile = ktile + Cfg::kTileBytes;
-
-    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int kk = 0; kk < KSTEPS; ++kk) {
-      const int col8 = 2 * (kk % 4) + k_col8;
-      const uint32_t addr =
-          ktile + (kk / 4) * Cfg::kBoxBytes + k_tok * 128 + ((col8 ^ (k_tok & 7)) << 4);
-      uint32_t a[4];
-      ldsm_x4(a, addr);
-      Op::run(sc, a, qb[kk][0], qb[kk][1]);
+    for (int c = 0; c < D / 8; ++c) {
+      const int h = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + h * Cfg::kQHalfBytes + qr * 128 +
+                                ((cc ^ (qr & 7)) << 4)) = use ? qv[c] : make_uint4(0u, 0u, 0u, 0u);
     }
-    const bool v0 = gi < nvalid, v1 = gi + 8 < nvalid;
-    float x[4];
-    x[0] = v0 ? sc[0] * p.qscale : -INFINITY;
-    x[1] = v0 ? sc[1] * p.qscale : -INFINITY;
-    x[2] = v1 ? sc[2] * p.qscale : -INFINITY;
-    x[3] = v1 ? sc[3] * p.qscale : -INFINITY;
-    float alpha[2], pr[4];
+    fence_proxy_async_smem();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot;
+  bool failed = false;
+
+  if (warp == Cfg::kProducerWarp) {
+    // ---- producer: key tile j into K stage j % NK, value tile j into V
+    //      stage j % NV.  Lane b < kBoxes copies box b (RB positions); a box
+    //      past the partition's end reads an out-of-range block, which the
+    //      copy fills with zeros.  Its table entry is read one tile ahead.
+    const uint64_t policy = policy_evict_first();
+    const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
+    auto entry = [&](int j) {
+      const int pos = j * KT + lane * RB;
+      return (lane < Cfg::kBoxes && j < n_tiles && pos < PS)
+                 ? make_int2(ld_nc(lrow + pos / BS), pos % BS)
+                 : make_int2(oob_block, 0);
+    };
+    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int2 e, uint32_t bar) {
+      if (lane < Cfg::kBoxes) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      float cm = fmaxf(x[h], x[h + 2]);
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 4));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 8));
-      cm = fmaxf(cm, __shfl_xor_sync(kFullMask, cm, 16));
-      const float mnew = fmaxf(m[h], cm);
-      alpha[h] = exp2f(m[h] - mnew);
-      pr[h] = exp2f(x[h] - mnew);
-      pr[h + 2] = exp2f(x[h + 2] - mnew);
-      float cs = pr[h] + pr[h + 2];
-      cs += __shfl_xor_sync(kFullMask, cs, 4);
-      cs += __shfl_xor_sync(kFullMask, cs, 8);
-      cs += __shfl_xor_sync(kFullMask, cs, 16);
-      l[h] = l[h] * alpha[h] + cs;
-      m[h] = mnew;
-    }
-    if (__any_sync(kFullMask, alpha[0] != 1.f || alpha[1] != 1.f)) {
-#pragma unroll
-      for (int i = 0; i < KSTEPS; ++i) {
-        acc[i][0] *= alpha[0];
-        acc[i][1] *= alpha[1];
-        acc[i][2] *= alpha[0];
-        acc[i][3] *= alpha[1];
+        for (int h = 0; h < Cfg::kHalves; ++h)
+          tma_load_4d(dst + h * Cfg::kKvHalfBytes + lane * RB * 128, map, h * 64, e.y, kvh, e.x,
+                      bar, policy);
       }
-    }
-    {
-      const int h0 = 2 * ti, h1 = 2 * ti + 1;
-      const uint16_t q0 = Op::bits(pr[0]), q1 = Op::bits(pr[1]);
-      const uint16_t q2 = Op::bits(pr[2]), q3 = Op::bits(pr[3]);
-      pt[h0 * C + gi] = q0;
-      pt[h1 * C + gi] = q1;
-      pt[h0 * C + gi + 8] = q2;
-      pt[h1 * C + gi + 8] = q3;
-      if constexpr (kSplitP) {
-        uint16_t* lo = pt + 8 * C;
-        lo[h0 * C + gi] = Op::bits(pr[0] - Op::back(q0));
-        lo[h1 * C + gi] = Op::bits(pr[1] - Op::back(q1));
-        lo[h0 * C + gi + 8] = Op::bits(pr[2] - Op::back(q2));
-        lo[h1 * C + gi + 8] = Op::bits(pr[3] - Op::back(q3));
+    };
+    int jk = 0, jv = 0;  // tiles whose key / value copies were issued
+    int2 cur = entry(0);
+    for (int j = 0; j < n_tiles; ++j) {
+      const int2 nxt = entry(j + 1);
+      const int sk = j % NK, sv = j % NV;
+      if (j >= NK &&
+          __any_sync(kFullMask, !mbar_wait(k_empty(sk), (uint32_t)(((j / NK) - 1) & 1)))) {
+        failed = true;
+        break;
       }
+      if (lane == 0) mbar_arrive_expect_tx(k_full(sk), Cfg::kKvBytes);
+      __syncwarp();
+      load_tile(&tmk, sbase + Cfg::kKRingOff + sk * Cfg::kKvBytes, cur, k_full(sk));
+      jk = j + 1;
+      if (j >= NV &&
+          __any_sync(kFullMask, !mbar_wait(v_empty(sv), (uint32_t)(((j / NV) - 1) & 1)))) {
+        failed = true;
+        break;
+      }
+      if (lane == 0) mbar_arrive_expect_tx(v_full(sv), Cfg::kKvBytes);
+      __syncwarp();
+      load_tile(&tmv, sbase + Cfg::kVRingOff + sv * Cfg::kKvBytes, cur, v_full(sv));
+      jv = j + 1;
+      cur = nxt;
     }
+    // Copies issued but possibly never consumed (another role stopped).
+    for (int j = jk - NK < 0 ? 0 : jk - NK; j < jk; ++j)
+      mbar_wait(k_full(j % NK), (uint32_t)((j / NK) & 1), kWaitLimitNs / 8);
+    for (int j = jv - NV < 0 ? 0 : jv - NV; j < jv; ++j)
+      mbar_wait(v_full(j % NV), (uint32_t)((j / NV) & 1), kWaitLimitNs / 8);
+  } else if (warp == Cfg::kMmaWarp) {
+    // ---- MMA issuer: S(0); per tile j, S(j+1) once its keys are in and the
+    //      softmax has read S(j), then P.V(j) once P(j) and the values are in.
+    // Descriptors are built once and stepped by constants (a descriptor's
+    // start address is its low 14 bits in 16-byte units; every operand lies
+    // below 256 KB).
+    auto wait_all = [&](uint32_t bar, int phase) {
+      const bool o = mbar_wait(bar, (uint32_t)(phase & 1));
+      return !__any_sync(kFullMask, !o);
+    };
+    const uint64_t qdesc = smem_desc_sw128(sbase + Cfg::kQOff, 16, 1024);
+    const uint64_t kdesc0 = smem_desc_sw128(sbase + Cfg::kKRingOff, 16, 1024);
+    // Values as copied, MN-major: 64-dim atoms kKvHalfBytes apart, 8-key
+    // groups 1024 B apart (with one atom, D = 64, the atom stride is unused).
+    const uint64_t vdesc0 = smem_desc_sw128(sbase + Cfg::kVRingOff,
+                                            Cfg::kHalves > 1 ? Cfg::kKvHalfBytes : 1024, 1024);
+    auto issue_s = [&](int j) {
+      if (lane == 0) {
+        const uint64_t kb = kdesc0 + (uint64_t)(((j % NK) * Cfg::kKvBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+          tc_mma_ss(tmem + Cfg::kSCol,
+                    qdesc + (uint64_t)((((kk >> 2) * Cfg::kQHalfBytes) + (kk & 3) * 32) >> 4),
+                    kb + (uint64_t)((((kk >> 2) * Cfg::kKvHalfBytes) + (kk & 3) * 32) >> 4),
+                    Cfg::kIdescS, kk > 0 ? 1u : 0u);
+        tc_commit(s_full);
+        tc_commit(k_empty(j % NK));
+      }
+      __syncwarp();
+    };
+    // P.V of tile j: keys 16kk .. 16kk+15 of P in columns 8kk .. 8kk+7 (a
+    // low part 32 columns on), value rows 16kk .. 16kk+15 2048 B apart.
+    auto issue_pv = [&](int j) {
+      if (lane == 0) {
+        const uint64_t vb = vdesc0 + (uint64_t)(((j % NV) * Cfg::kKvBytes) >> 4);
+        const uint32_t dcol = tmem + Cfg::kOCol, pa = tmem + Cfg::kPCol;
+#pragma unroll
+        for (int kk = 0; kk < KT / 16; ++kk) {
+          tc_mma_ts(dcol, pa + 8 * kk, vb + 128 * kk, Cfg::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if constexpr (Cfg::kTwoPartP)
+            tc_mma_ts(dcol, pa + 32 + 8 * kk, vb + 128 * kk, Cfg::kIdescPV, 1u);
+        }
+        tc_commit(p_free);
+        tc_commit(v_empty(j % NV));
+      }
+      __syncwarp();
+    };
+    bool ok = wait_all(k_full(0), 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0);
+    }
+    for (int j = 0; j < n_tiles && ok; ++j) {
+      if (j + 1 < n_tiles) {
+        ok = wait_all(k_full((j + 1) % NK), (j + 1) / NK) && wait_all(s_free, j);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(j + 1);
+      }
+      ok = wait_all(p_full, j) && wait_all(v_full(j % NV), j / NV);
+      if (!ok) break;
+      tc_fence_after();
+      issue_pv(j);
+    }
+    if (ok && lane == 0) tc_commit(o_last);
+    failed = !ok;
+    // Every MMA this thread issued has completed before the tensor memory
+    // is released.
+    if (lane == 0) tc_commit(drain);
     __syncwarp();
-    const uint32_t* ptw = reinterpret_cast<const uint32_t*>(pt);
-    const uint32_t bh0 = ptw[(gi * C + 2 * ti) / 2];
-    const uint32_t bh1 = ptw[(gi * C + 2 * ti + 8) / 2];
-    uint32_t bl0 = 0, bl1 = 0;
-    if constexpr (kSplitP) {
-      bl0 = ptw[(8 * C + gi * C + 2 * ti) / 2];
-      bl1 = ptw[(8 * C + gi * C + 2 * ti + 8) / 2];
+    mbar_wait(drain, 0);
+  } else if (warp < nsw) {
+    // ---- softmax: copy cp of row r_local, keys cp * KW .. cp * KW + KW - 1 ---
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    // Scores are taken as s * |factor| with the sign folded into s, so the
+    // row maximum can be found on the raw scores.
+    const bool qneg = p.qscale < 0.f;
+    const float qscale = fabsf(p.qscale);
+    float m = -INFINITY, l = 0.f;  // l: this copy's part of the row's sum
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      ok = mbar_wait(s_full, (uint32_t)(j & 1));
+      if (__any_sync(kFullMask, !ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t x[KW];
+      {
+        uint32_t w[KT];
+        tmem_ld64(lane_base + Cfg::kSCol, w);
+#pragma unroll
+        for (int i = 0; i < KW; ++i) {
+          uint32_t v = w[i];
+#pragma unroll
+          for (int cc = 1; cc < DUP; ++cc)
+            if (cp == cc) v = w[cc * KW + i];
+          x[i] = v;
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(s_free);
+      if (qneg) {
+#pragma unroll
+        for (int i = 0; i < KW; ++i) x[i] ^= 0x80000000u;
+      }
+      // Positions past the partition's end (a last tile of fewer than 64).
+      const int lim = PS - j * KT - cp * KW;
+      if (lim < KW) {
+#pragma unroll
+        for (int i = 0; i < KW; ++i)
+          if (i >= lim) x[i] = __float_as_uint(-INFINITY);
+      }
+      float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int i = 0; i < KW; i += 8)
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          mq[u] = max3(mq[u], __uint_as_float(x[i + 2 * u]), __uint_as_float(x[i + 2 * u + 1]));
+      float mraw = max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+#pragma unroll
+      for (int sh = 1; sh < DUP; sh <<= 1) mraw = fmaxf(mraw, __shfl_xor_sync(kFullMask, mraw, sh));
+      const float mx = mraw * qscale;
+      // Lazy maximum: raise it (and rescale O and l) only when the tile's
+      // maximum exceeds it by more than 8 (P <= 2^8 otherwise).  Tile 0
+      // always holds a position of the partition, so m is finite after it.
+      // The copies of a row see the same maximum and decide alike.
+      bool rescale = false;
+      float alpha = 1.f;
+      if (j == 0) {
+        m = mx;
+      } else {
+        const bool raise = mx > m + 8.f;
+        rescale = __any_sync(kFullMask, raise);
+        if (raise) {
+          alpha = ex2(m - mx);
+          l *= alpha;
+          m = mx;
+        }
+      }
+      // Weights 2^(s * scale - m); positions past the partition's end get 0
+      // (set after the exponential, so that a zero scale cannot make NaN).
+      const float2 qs2 = make_float2(qscale, qscale), nm2 = make_float2(-m, -m);
+      float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+      for (int i = 0; i < KW; i += 2) {
+        const float2 a =
+            __ffma2_rn(make_float2(__uint_as_float(x[i]), __uint_as_float(x[i + 1])), qs2, nm2);
+        const float2 e = make_float2(i < lim ? ex2(a.x) : 0.f, i + 1 < lim ? ex2(a.y) : 0.f);
+        x[i] = __float_as_uint(e.x);
+        x[i + 1] = __float_as_uint(e.y);
+        sum2[(i >> 1) & 1] = __fadd2_rn(sum2[(i >> 1) & 1], e);
+      }
+      const float2 sx = __fadd2_rn(sum2[0], sum2[1]);
+      l += sx.x + sx.y;
+      // P: keys 2c, 2c+1 in column c, this copy's keys only (zeros for the
+      // other copies' keys).  bf16: the truncated weights, and in column
+      // 32 + c the exact remainders rounded to bf16; fp16: one part.
+      uint32_t hi[KW / 2], lo[KW / 2];
+#pragma unroll
+      for (int c = 0; c < KW / 2; ++c) {
+        const uint32_t a = x[2 * c], b = x[2 * c + 1];
+        if constexpr (Cfg::kTwoPartP) {
+          hi[c] = __byte_perm(a, b, 0x7632);
+          const float2 r = __ffma2_rn(
+              make_float2(__uint_as_float(a & 0xFFFF0000u), __uint_as_float(b & 0xFFFF0000u)),
+              make_float2(-1.f, -1.f), make_float2(__uint_as_float(a), __uint_as_float(b)));
+          lo[c] = pack_pair<__nv_bfloat16>(r.x, r.y);
+        } else {
+          hi[c] = pack_pair<__half>(__uint_as_float(a), __uint_as_float(b));
+          lo[c] = 0u;
+        }
+      }
+      uint32_t pk[KT];
+#pragma unroll
+      for (int c = 0; c < KT / 2; ++c) {
+        const bool mine = c / (KW / 2) == cp;
+        pk[c] = mine ? hi[c % (KW / 2)] : 0u;
+        pk[KT / 2 + c] = mine ? lo[c % (KW / 2)] : 0u;
+      }
+      // P.V of tile j-1 has read P and added into O before either changes.
+      if (j > 0) {
+        ok = mbar_wait(p_free, (uint32_t)((j - 1) & 1));
+        if (__any_sync(kFullMask, !ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      if constexpr (Cfg::kTwoPartP) {
+        tmem_st64(lane_base + Cfg::kPCol, pk);
+      } else {
+        tmem_st32(lane_base + Cfg::kPCol, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+      }
+      if (rescale) {
+#pragma unroll 1
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(lane_base + Cfg::kOCol + c4 * 32, o);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(p_full);
     }
+    if (ok) ok = !__any_sync(kFullMask, !mbar_wait(o_last, 0));
+    failed = !ok;
+    if (ok) {
+      tc_fence_after();
+      // The row's sum and O: the copies' parts added together.  O is summed
+      // by halving exchanges, after which copy cp holds dims cp * DW .. +
+      // DW - 1 of each 32-dim chunk, the ones it writes.
 #pragma unroll
-    for (int i = 0; i < KSTEPS; ++i) {
-      const int col8 = 2 * (i % 4) + v_col8;
-      const uint32_t addr =
-          vtile + (i / 4) * Cfg::kBoxBytes + v_tok * 128 + ((col8 ^ (v_tok & 7)) << 4);
-      uint32_t a[4];
-      ldsm_x4_trans(a, addr);
-      Op::run(acc[i], a, bh0, bh1);
-      if constexpr (kSplitP) Op::run(acc[i], a, bl0, bl1);
-    }
-    __syncwarp();  // this warp is done with the stage and with P^T
-    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
-  }
-  if (timed_out && lane == 0) set_error(p.err, PKV_DEV_TIMEOUT);
-
-  // ---- this warp's rows: (m, l) and o = acc / l, or the invalid marker ------
-  // Lane (gi, ti) holds dims 16i + gi (+ 8) of columns 2ti and 2ti + 1.
+      for (int sh = 1; sh < DUP; sh <<= 1) l += __shfl_xor_sync(kFullMask, l, sh);
+#pragma unroll 1
+      for (int c4 = 0; c4 < D / 32; ++c4) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + Cfg::kOCol + c4 * 32, o);
+        int n = 32;
 #pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int col = 2 * ti + h;
-    const int s = row_seq(col);
-    const int st = row_status(s);
-    if (st == 0) continue;
-    const bool broken = st < 0 || bad || timed_out;
-    if (st < 0 && gi == 0) set_error(p.err, PKV_DEV_SHARING);
-    const int head = kvh * G + (rb * Cfg::kRows + warp * 8 + col) % G;
-    const int L = ld_nc(p.seq_lens + s);
-    const int nparts = (L + PS - 1) / PS;
-    const float inv = 1.f / l[h];
-    if (nparts == 1) {  // the whole sequence is this partition: final output
-      T* orow = out + ((int64_t)s * H + head) * D;
+        for (int sh = DUP / 2; sh >= 1; sh >>= 1) {
+          const bool upper = (cp & sh) != 0;
+          n >>= 1;
 #pragma unroll
-      for (int i = 0; i < KSTEPS; ++i)
+          for (int i = 0; i < 16; ++i) {
+            if (i < n) {
+              const uint32_t keep = upper ? o[n + i] : o[i];
+              const uint32_t give = upper ? o[i] : o[n + i];
+              o[i] = __float_as_uint(__uint_as_float(keep) +
+                                     __uint_as_float(__shfl_xor_sync(kFullMask, give, sh)));
+            }
+          }
+        }
+        uint32_t v[DW];
 #pragma unroll
-        for (int half = 0; half < 2; ++half)
-          orow[16 * i + gi + 8 * half] = Elem<T>::from_f(broken ? 0.f : acc[i][2 * half + h] * inv);
+        for (int i = 0; i < DW; ++i) v[i] = o[i];
+        if (has_row && my_status == 1) store_row(false, m, l, v, c4 * 32 + cp * DW);
+      }
+      mark_broken_rows(false);
     } else {
-      const int64_t w = ((int64_t)s * H + head) * p.num_parts + part;
-#pragma unroll
-      for (int i = 0; i < KSTEPS; ++i)
-#pragma unroll
-        for (int half = 0; half < 2; ++half)
-          p.ws_o[w * D + 16 * i + gi + 8 * half] = broken ? 0.f : acc[i][2 * half + h] * inv;
-      if (gi == 0) p.ws_ml[w] = broken ? make_float2(-INFINITY, -1.f) : make_float2(m[h], l[h]);
+      mark_broken_rows(true);
     }
   }
+
+  // ---- release the tensor memory ------------------------------------------
+  if (failed && lane == 0) set_error(p.err, PKV_DEV_TIMEOUT);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == Cfg::kProducerWarp) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
 }  // namespace pkv

@@ -173,33 +173,6 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
-// Largest of three.
-__device__ __forceinline__ float max3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// 2^x with the hardware approximation (flushes results below 2^-126 to 0).
-__device__ __forceinline__ float ex2(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-template <typename T>
-__device__ __forceinline__ uint32_t pack_pair(float lo, float hi);
-template <>
-__device__ __forceinline__ uint32_t pack_pair<__half>(float lo, float hi) {
-  const __half2 h = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-template <>
-__device__ __forceinline__ uint32_t pack_pair<__nv_bfloat16>(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-
 template <typename T, int D, int BS, int G, bool KV8>
 __global__ void __launch_bounds__(PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>::kThreads,
                                   PrefillTcCfg<T, D, BS, G, kPrefillQTiles, KV8>::kCtasPerSm)

@@ -116,15 +116,17 @@ def test_block_copy_argument_errors(lib):
 def test_shared_decode_argument_errors(lib):
     # Group arguments are checked on the host before anything else.
     c = fake_cache()
-    args = lambda starts, prefix, ng, mg: (ctypes.byref(c), P(0x10000), P(0x20000), 4, P(0x30000), 8,
-                                            8, 0, ctypes.c_float(0.1), P(0x40000), starts, prefix, ng,
-                                            mg, P(0), 0, 0, None)
+    args = lambda starts, prefix, ng, mg, tail=0: (ctypes.byref(c), P(0x10000), P(0x20000), 4,
+                                                    P(0x30000), 8, 8, 0, ctypes.c_float(0.1),
+                                                    P(0x40000), starts, prefix, ng, mg, tail, P(0),
+                                                    0, 0, None)
     assert lib.paged_attention_decode_shared(*args(P(0), P(0x50000), 2, 4)) == -1
     assert lib.paged_attention_decode_shared(*args(P(0x60000), P(0), 2, 4)) == -1
     assert lib.paged_attention_decode_shared(*args(P(0x60002), P(0x50000), 2, 4)) == -4
     assert lib.paged_attention_decode_shared(*args(P(0x60000), P(0x50000), -1, 4)) == -3
     assert lib.paged_attention_decode_shared(*args(P(0x60000), P(0x50000), 2, 0)) == -3
     assert lib.paged_attention_decode_shared(*args(P(0x60000), P(0x50000), 2, 9)) == -3
+    assert lib.paged_attention_decode_shared(*args(P(0x60000), P(0x50000), 2, 4, -1)) == -3
 
 
 def test_read_stream_argument_errors(lib):

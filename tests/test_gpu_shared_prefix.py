@@ -4,7 +4,10 @@ the oracle: groups of sequences whose tables share their first blocks
 table; the parallel-sampling workload at full size with all 128 sequences;
 identical forks stay bit-identical; relabelling the pool is bit-exact; a
 member that breaks its group's contract is flagged and zeroed; sequences
-outside every group and pools without group support decode in full."""
+outside every group and pools without group support decode in full; the
+partition pass's tail grid (tail_parts) gives the full grid's bits (one
+slice: merged in place, against the oracle) and flags the sequences it does
+not cover."""
 
 import numpy as np
 import pytest
@@ -57,7 +60,7 @@ class GroupCase:
         self.q = torch.randn(len(self.lens), Hk * G, D, generator=g).to(TORCH[dtype])
         self.scale = 1.0 / np.sqrt(D)
 
-    def run(self, part=0, plain=False, tables=None, k=None, v=None, q=None):
+    def run(self, part=0, plain=False, tables=None, k=None, v=None, q=None, tail_parts=0):
         cache = pkv.PagedKVCache((self.k if k is None else k).cuda(),
                                  (self.v if v is None else v).cuda())
         tab = torch.from_numpy(self.tables if tables is None else tables).cuda()
@@ -68,7 +71,8 @@ class GroupCase:
         else:
             out = pkv.paged_attention_decode_shared(
                 cache, qq, tab, ln, self.scale, torch.from_numpy(self.starts).cuda(),
-                torch.from_numpy(self.prefixes).cuda(), self.max_group, partition_size=part)
+                torch.from_numpy(self.prefixes).cuda(), self.max_group, partition_size=part,
+                tail_parts=tail_parts)
         return out, pkv.paged_get_device_error()
 
     def oracle(self):
@@ -138,6 +142,12 @@ def test_parallel_sampling_workload_full_size_all_sequences():
     got = gpu_out_f64(out)
     assert np.all(np.isfinite(got))
     assert float(np.max(np.abs(got - ref))) <= TOL["bf16"]
+    # Every fork's tail (the prompt's last 7 tokens and the new one) lies in
+    # one partition: a one-slice tail grid, merged in place, on all 128.
+    out1 = pkv.paged_attention_decode_shared(cache, data.q.to(dev), tables, lens, data.scale, starts,
+                                             prefixes, seqs.forks, partition_size=part, tail_parts=1)
+    assert pkv.paged_get_device_error() == 0
+    assert float(np.max(np.abs(gpu_out_f64(out1) - ref))) <= TOL["bf16"]
 
 
 def test_identical_forks_are_bit_identical():
@@ -221,3 +231,57 @@ def test_fp8_pool_decodes_in_full():
     bb = pkv.paged_attention_decode(cache, q, tables, lens, 0.088)
     assert pkv.paged_get_device_error() == 0
     assert torch.equal(a, bb)
+
+
+@pytest.mark.parametrize("dt", ["bf16", "f16"])
+def test_tail_grid(dt):
+    # Tails: group 0 (prefix 128 = two 64-position partitions) ends in
+    # partition 2, group 1 (prefix 192) in partition 3, group 2 (prefix 64)
+    # in partition 1: one slice covers every sequence.  Member 0 of group 3
+    # has no tail (length = prefix = 128: the CTA merges the two shared
+    # partitions alone), group 4's member is one shared partition (written
+    # by the shared-prefix kernel).  Two or more slices give the full
+    # grid's bits; one slice merges in place.
+    groups = [(3, 128, [140, 150, 191]), (4, 192, [200, 230, 250, 255]), (1, 64, [100]),
+              (2, 128, [128, 129]), (1, 64, [64])]
+    c = GroupCase(dt, 2, 4, 128, 16, groups, seed=23)
+    full, err = c.run(part=64)
+    assert err == 0
+    got, ref = gpu_out_f64(full), c.oracle()
+    assert np.all(np.abs(got - ref) <= edge_tol(dt, ref))
+    for tp in (2, 9):
+        out, err = c.run(part=64, tail_parts=tp)
+        assert err == 0
+        assert torch.equal(out.cpu(), full.cpu())
+    out, err = c.run(part=64, tail_parts=1)
+    assert err == 0
+    assert np.all(np.abs(gpu_out_f64(out) - ref) <= edge_tol(dt, ref))
+
+
+def test_tail_grid_flags_uncovered_sequences():
+    # With 64-position partitions: members of length 200 and 250 (prefix
+    # 128) need partitions 2 and 3; sequence 6 (outside every group, length
+    # 150) needs partitions 0-2.  A one-slice tail grid zeroes and flags
+    # exactly those; three slices cover everyone.
+    groups = [(3, 128, [140, 200, 250]), (2, 64, [70, 80]), (2, 0, [30, 150])]
+    c = GroupCase("bf16", 2, 4, 128, 16, groups, seed=29)
+    c.starts = np.asarray([0, 3, 5], dtype=np.int32)
+    c.prefixes = np.asarray([128, 64], dtype=np.int32)
+    ref = c.oracle()
+    out, err = c.run(part=64, tail_parts=1)
+    assert err & _lib.PKV_DEV_SHARING
+    got = gpu_out_f64(out)
+    uncovered, covered = [1, 2, 6], [0, 3, 4, 5]
+    assert np.all(got[uncovered] == 0.0)
+    assert np.all(np.abs(got[covered] - ref[covered]) <= edge_tol("bf16", ref[covered]))
+    out, err = c.run(part=64, tail_parts=3)
+    assert err == 0
+    assert np.all(np.abs(gpu_out_f64(out) - ref) <= edge_tol("bf16", ref))
+    # Two slices (merge launch): the same rows zeroed, as member 1 and 2
+    # need two tail partitions and sequence 6 three.
+    out, err = c.run(part=64, tail_parts=2)
+    assert err & _lib.PKV_DEV_SHARING
+    got = gpu_out_f64(out)
+    assert np.all(got[[6]] == 0.0)
+    ok = [0, 1, 2, 3, 4, 5]
+    assert np.all(np.abs(got[ok] - ref[ok]) <= edge_tol("bf16", ref[ok]))
