@@ -51,22 +51,25 @@ from paged_kv_cache_145_gb300 import synth  # noqa: E402
 
 METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
 
-# DRAM bytes (read + write) per launch of the decode partition kernel, from
+# DRAM bytes (read + write) per launch of the decode partition kernel (for
+# the shared-prefix decode: of its three kernels together, per call), from
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, KV
-# dtype and partition length, with the hash of the sources of that kernel
-# family they were taken on.  A stale hash reports null.
+# dtype or decode form, and partition length, with the hash of the sources
+# of that kernel family they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b/native/512": (1277883392, "212a013fc36964d1"),
-    "gqa/native/512": (1127114752, "212a013fc36964d1"),
-    "opt13b/fp8/2048": (641348352, "fc43370ae5b670a4"),
-    "gqa/fp8/2048": (563023616, "fc43370ae5b670a4"),
-    "long/native/512": (875519232, "212a013fc36964d1"),
-    "long/fp8/1536": (437342976, "fc43370ae5b670a4"),
-    "fork/native/512": (77156608, "212a013fc36964d1"),
+    "opt13b/native/512": (1277835136, "452345e63fe421e3"),
+    "gqa/native/512": (1127102976, "452345e63fe421e3"),
+    "long/native/512": (875536640, "452345e63fe421e3"),
+    "fork/native/512": (77182720, "452345e63fe421e3"),
+    "fork/shared/512": (79988736, "452345e63fe421e3"),
+    "opt13b/fp8/2048": (641391232, "54e1ddb323cddf15"),
+    "gqa/fp8/2048": (563100160, "54e1ddb323cddf15"),
+    "long/fp8/1536": (437307904, "54e1ddb323cddf15"),
 }
 
 KERNEL_SOURCES = {
-    "native": ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh"),
+    "native": ("common.cuh", "decode.cuh", "decode_mma.cuh", "decode_launch.cuh",
+               "decode_shared.cuh", "tcgen05.cuh"),
     "fp8": ("common.cuh", "decode.cuh", "decode_mma_fp8.cuh", "decode_launch.cuh"),
 }
 
@@ -995,7 +998,7 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
     layers = w.cfg.get("layers", 1)
     src_hash = kernel_source_hash("fp8" if kv_dtype else "native")
     default_shape = args.partition == 0 and args.block_size == 0 and args.table == "shuffled"
-    key = "%s/%s/%d" % (name, "fp8" if kv_dtype else "native", part)
+    key = "%s/%s/%d" % (name, "fp8" if kv_dtype else ("shared" if shared else "native"), part)
     tr = TRAFFIC.get(key) if default_shape else None
     traffic = tr[0] if tr and tr[1] == src_hash else None
     line = {
