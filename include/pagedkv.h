@@ -273,8 +273,10 @@ int paged_attention_prefill(const pkv_cache* cache, const void* q, int64_t total
  *                  group's shared ones (from partition 0 for a sequence
  *                  outside every group); a sequence that needs more gets a
  *                  zero output row and sets PKV_DEV_SHARING.  With forks
- *                  whose tails fit in one partition, 1 launches one CTA per
- *                  (sequence, KV head) instead of one per partition.
+ *                  whose tails fit in one partition, 1 computes each tail
+ *                  and merges it with the shared partials in one small
+ *                  pass per (sequence, KV head), in place of the partition
+ *                  pass and the merge.
  *   workspace      as for paged_attention_decode (same size).
  *
  * A member whose table or length breaks its group's contract gets a zero

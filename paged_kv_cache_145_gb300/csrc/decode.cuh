@@ -81,8 +81,9 @@ struct DecodeParams {
   int num_groups;
   int num_seqs;
   // Partition pass of the shared-prefix decode: 0, slice z is partition z
-  // (the shared ones exit); tail_parts > 0, the grid has tail_parts slices
-  // and slice z is the z-th partition after the sequence's shared ones.
+  // (the shared ones exit); tail_parts > 1, the grid has tail_parts slices
+  // and slice z is the z-th partition after the sequence's shared ones;
+  // 1, decode_tail_merge_kernel replaces the partition pass and the merge.
   int tail_parts;
 };
 

@@ -61,9 +61,7 @@ int launch_decode_cfg(const DecodeParams& p, int num_seqs, const DecodeMaps* map
             (unsigned)(p.tail_parts > 0 ? p.tail_parts : p.num_parts));
   bool launched = false;
   if constexpr (mma_eligible<T, D, BS, G>()) {
-    // A one-slice tail grid (short tails, one CTA per sequence and KV head)
-    // runs on the CUDA-core kernel: more of its CTAs fit on an SM.
-    if (maps && p.tail_parts != 1) {
+    if (maps) {
       using Cfg = MmaCfg<T, D, BS, G>;
       auto kern = decode_partition_mma_kernel<T, D, BS, G>;
       if (allow_smem<Cfg>(kern, Cfg::kMaxSmem) != PKV_OK) return PKV_ERR_CUDA;
@@ -108,6 +106,11 @@ int launch_shared_cfg(const DecodeParams& p, int num_seqs, int max_group_size,
                      ? launch_shared_dup<T, D, BS, G, 4>(p, max_group_size, maps, stream)
                      : launch_shared_dup<T, D, BS, G, 1>(p, max_group_size, maps, stream);
   if (rc != PKV_OK) return rc;
+  if (p.tail_parts == 1) {  // every tail in one partition: tail and merge in one pass
+    decode_tail_merge_kernel<T, D, BS, G>
+        <<<dim3((unsigned)p.kv_heads, (unsigned)num_seqs), 128, 0, stream>>>(p);
+    return cudaPeekAtLastError() == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+  }
   return launch_decode_cfg<T, D, BS, G>(p, num_seqs, part_maps, stream);
 }
 

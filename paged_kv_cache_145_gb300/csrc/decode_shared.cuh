@@ -617,4 +617,214 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
   if (warp == Cfg::kProducerWarp) tmem_dealloc(tmem, Cfg::kTmemCols);
 }
 
+// Tail and merge for a one-slice tail grid (tail_parts = 1): every
+// sequence's positions past its group's shared partitions lie in one
+// partition (for a sequence outside every group: the whole sequence in
+// one partition).  One CTA per (KV head, sequence), four warps, warp w
+// taking query heads kvh * G + h for h = w, w + 4: it computes the tail's
+// partial on CUDA cores (a warp-wide dot product per position, eight
+// positions' rows loaded at a time), merges it with the shared-prefix
+// kernel's partials in the workspace (M = max m_p, w_p = l_p 2^(m_p - M),
+// out = sum w_p o_p / sum w_p, partitions in order, then the tail), and
+// writes the output.  This replaces the partition pass and the merge
+// launch.  A sequence whose tail needs more than one partition, or whose
+// length or tail table entries are invalid, gets zero rows and its error
+// bit (PKV_DEV_SHARING, PKV_DEV_SEQ_LEN, PKV_DEV_TABLE_RANGE).
+template <typename T, int D, int BS, int G>
+__global__ void __launch_bounds__(128) decode_tail_merge_kernel(const DecodeParams p) {
+  constexpr int DPL = D / 32;  // dims per lane
+  constexpr int NB = 8;        // positions per batch of row loads
+  constexpr int NPRE = 2;      // shared partials loaded ahead (the rest in the merge loop)
+  constexpr int HPW = (G + 3) / 4;  // query heads per warp
+  static_assert(sizeof(T) == 2 && DPL % 2 == 0, "16-bit pools");
+  __shared__ int ent[kMaxPartSize / BS + 1];
+  const int kvh = blockIdx.x;
+  const int s = blockIdx.y;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = p.num_heads;
+  const int PS = p.part_size;
+  T* out = static_cast<T*>(p.out);
+  const int64_t out0 = ((int64_t)s * H + (int64_t)kvh * G) * D;
+  // Issued together: the length, the group search, this warp's query rows.
+  const int L = ld_nc(p.seq_lens + s);
+  float q[HPW][DPL];
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int g = warp + 4 * hh;
+    if (g < G)
+      RowLoad<T, DPL>::load(static_cast<const T*>(p.q) + ((int64_t)s * H + kvh * G + g) * D +
+                                lane * DPL, q[hh]);
+  }
+  const int first = shared_parts_of(p, s);  // partitions the shared-prefix kernel computed
+  auto zero_rows = [&]() {
+    for (int e = threadIdx.x; e < G * D; e += 128) out[out0 + e] = Elem<T>::from_f(0.f);
+  };
+  if (L < 1 || L > p.max_len) {
+    zero_rows();
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SEQ_LEN);
+    return;
+  }
+  const int nparts = (L + PS - 1) / PS;
+  const int tok0 = first * PS;
+  if (nparts == 1 && first >= 1) return;  // the shared-prefix kernel wrote the output
+  if (tok0 < L && first + 1 < nparts) {   // the tail needs more than one partition
+    zero_rows();
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_SHARING);
+    return;
+  }
+  const int nprev = min(first, nparts);  // partials in the workspace
+  // Issued together: the tail's table entries (positions tok0 .. L - 1) and
+  // the first shared partials of this warp's heads.
+  const int tail = max(L - tok0, 0);
+  const int blk0 = tok0 / BS;
+  const int nblk = (tail + BS - 1) / BS;
+  int bad = 0;
+  for (int i = threadIdx.x; i < nblk; i += 128) {
+    const int e = ld_nc(p.tables + (int64_t)s * p.max_blocks + blk0 + i);
+    bad |= (e < 0 || (int64_t)e >= p.num_blocks);
+    ent[i] = e;
+  }
+  float2 pml[HPW][NPRE];
+  float po[HPW][NPRE][DPL];
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int64_t row0 = ((int64_t)s * H + kvh * G + warp + 4 * hh) * p.num_parts;
+#pragma unroll
+    for (int k = 0; k < NPRE; ++k) {
+      if (warp + 4 * hh < G && k < nprev) {
+        pml[hh][k] = p.ws_ml[row0 + k];
+        RowLoad<float, DPL>::load(p.ws_o + (row0 + k) * D + lane * DPL, po[hh][k]);
+      }
+    }
+  }
+  if (__syncthreads_or(bad)) {
+    zero_rows();
+    if (threadIdx.x == 0) set_error(p.err, PKV_DEV_TABLE_RANGE);
+    return;
+  }
+  const T* kc = static_cast<const T*>(p.k_cache);
+  const T* vc = static_cast<const T*>(p.v_cache);
+#pragma unroll
+  for (int hh = 0; hh < HPW; ++hh) {
+    const int g = warp + 4 * hh;
+    if (g >= G) break;
+    const int head = kvh * G + g;
+    // ---- the tail's partial (m, l, o) in base-2 units ----------------------
+    float m = -INFINITY, l = 0.f, o[DPL];
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) o[i] = 0.f;
+    for (int t0 = 0; t0 < tail; t0 += NB) {
+      // This lane's DPL elements of NB key and value rows, kept packed
+      // (two 16-bit elements per word) until used.
+      constexpr int W = DPL / 2;
+      uint32_t kr[NB][W], vr[NB][W];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const int t = min(t0 + u, tail - 1);  // past the tail: a repeat, weighted 0 below
+        const int64_t row = ((int64_t)ent[t / BS] * p.kv_heads + kvh) * BS + (tok0 + t) % BS;
+        const uint32_t* kp = reinterpret_cast<const uint32_t*>(kc + row * D + lane * DPL);
+        const uint32_t* vp = reinterpret_cast<const uint32_t*>(vc + row * D + lane * DPL);
+        if constexpr (W == 2) {
+          const uint2 a = *reinterpret_cast<const uint2*>(kp), b = *reinterpret_cast<const uint2*>(vp);
+          kr[u][0] = a.x; kr[u][1] = a.y; vr[u][0] = b.x; vr[u][1] = b.y;
+        } else {
+#pragma unroll
+          for (int w = 0; w < W; ++w) {
+            kr[u][w] = kp[w];
+            vr[u][w] = vp[w];
+          }
+        }
+      }
+      float x[NB];
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        float d = 0.f;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float2 kf = Elem<T>::pair(kr[u][w]);
+          d = fmaf(q[hh][2 * w], kf.x, d);
+          d = fmaf(q[hh][2 * w + 1], kf.y, d);
+        }
+        x[u] = d;
+      }
+#pragma unroll
+      for (int sh = 16; sh >= 1; sh >>= 1)
+#pragma unroll
+        for (int u = 0; u < NB; ++u) x[u] += __shfl_xor_sync(kFullMask, x[u], sh);
+      float mb = -INFINITY;
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        x[u] = t0 + u < tail ? x[u] * p.qscale : -INFINITY;
+        mb = fmaxf(mb, x[u]);
+      }
+      const float mnew = fmaxf(m, mb);
+      const float alpha = exp2f(m - mnew);  // 0 on the first batch (m = -inf)
+      l *= alpha;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) o[i] *= alpha;
+#pragma unroll
+      for (int u = 0; u < NB; ++u) {
+        const float pw = exp2f(x[u] - mnew);
+        l += pw;
+#pragma unroll
+        for (int w = 0; w < W; ++w) {
+          const float2 vf = Elem<T>::pair(vr[u][w]);
+          o[2 * w] = fmaf(pw, vf.x, o[2 * w]);
+          o[2 * w + 1] = fmaf(pw, vf.y, o[2 * w + 1]);
+        }
+      }
+      m = mnew;
+    }
+    // ---- merge with the shared partials, in order, then the tail -----------
+    // A partial's o is normalised (its weights sum to 1); the tail's is not.
+    const int64_t row0 = ((int64_t)s * H + head) * p.num_parts;
+    float big = m;
+    bool broken = false;
+#pragma unroll
+    for (int k = 0; k < NPRE; ++k) {
+      if (k < nprev) {
+        broken |= pml[hh][k].y < 0.f;
+        big = fmaxf(big, pml[hh][k].x);
+      }
+    }
+    for (int k = NPRE; k < nprev; ++k) {
+      const float2 v = p.ws_ml[row0 + k];
+      broken |= v.y < 0.f;
+      big = fmaxf(big, v.x);
+    }
+    float acc[DPL];
+    float den = 0.f;
+#pragma unroll
+    for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+#pragma unroll
+    for (int k = 0; k < NPRE; ++k) {
+      if (k < nprev) {
+        const float wgt = pml[hh][k].y * exp2f(pml[hh][k].x - big);
+        den += wgt;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = fmaf(po[hh][k][i], wgt, acc[i]);
+      }
+    }
+    for (int k = NPRE; k < nprev; ++k) {
+      const float2 v = p.ws_ml[row0 + k];
+      const float wgt = v.y * exp2f(v.x - big);
+      den += wgt;
+      float ov[DPL];
+      RowLoad<float, DPL>::load(p.ws_o + (row0 + k) * D + lane * DPL, ov);
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] = fmaf(ov[i], wgt, acc[i]);
+    }
+    if (tail > 0) {
+      const float wt = exp2f(m - big);
+      den += l * wt;
+#pragma unroll
+      for (int i = 0; i < DPL; ++i) acc[i] = fmaf(o[i], wt, acc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < DPL; ++i)
+      out[out0 + (int64_t)g * D + lane * DPL + i] = Elem<T>::from_f(broken ? 0.f : acc[i] / den);
+  }
+}
+
 }  // namespace pkv

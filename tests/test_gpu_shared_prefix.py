@@ -157,18 +157,20 @@ def test_identical_forks_are_bit_identical():
     c = GroupCase("bf16", 2, 4, 128, 16, groups, seed=9)
     c.tables[1:] = c.tables[0]
     c.q[1:] = c.q[0]
-    out, err = c.run(part=64)
-    assert err == 0
-    o = out.cpu()
-    for i in range(1, 8):
-        assert torch.equal(o[i], o[0])
+    for tp in (0, 1):
+        out, err = c.run(part=64, tail_parts=tp)
+        assert err == 0
+        o = out.cpu()
+        for i in range(1, 8):
+            assert torch.equal(o[i], o[0])
 
 
-def test_relabelling_blocks_is_bit_exact():
-    groups = [(4, 160, [170, 200, 161, 300]), (2, 32, [40, 90])]
+@pytest.mark.parametrize("groups,tps", [
+    ([(4, 160, [170, 200, 161, 300]), (2, 32, [40, 90])], (0, 3)),
+    ([(4, 128, [130, 150, 170, 191]), (2, 64, [70, 100])], (0, 1, 2)),
+])
+def test_relabelling_blocks_is_bit_exact(groups, tps):
     c = GroupCase("f16", 2, 4, 128, 16, groups, seed=11)
-    out0, err = c.run(part=64)
-    assert err == 0
     perm = np.random.default_rng(3).permutation(c.N)
     inv = np.argsort(perm)
     k2, v2 = torch.empty_like(c.k), torch.empty_like(c.v)
@@ -176,9 +178,12 @@ def test_relabelling_blocks_is_bit_exact():
     v2[torch.from_numpy(perm)] = c.v
     tables = np.where(c.tables >= 0, perm[np.maximum(c.tables, 0)], -1).astype(np.int32)
     assert np.array_equal(inv[perm], np.arange(c.N))
-    out1, err = c.run(part=64, tables=tables, k=k2, v=v2)
-    assert err == 0
-    assert torch.equal(out0.cpu(), out1.cpu())
+    for tp in tps:
+        out0, err = c.run(part=64, tail_parts=tp)
+        assert err == 0
+        out1, err = c.run(part=64, tables=tables, k=k2, v=v2, tail_parts=tp)
+        assert err == 0
+        assert torch.equal(out0.cpu(), out1.cpu())
 
 
 def test_broken_member_is_flagged_and_zeroed():
