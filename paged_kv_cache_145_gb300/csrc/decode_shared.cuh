@@ -197,6 +197,69 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
   for (int i = threadIdx.x; i < Cfg::kRows; i += Cfg::kThreads) member_bad[i] = 0;
   __syncthreads();
 
+  // ---- producer: key tile j into K stage j % NK, value tile j into V stage
+  //      j % NV.  Lane b < kBoxes copies box b (RB positions); a box past the
+  //      partition's end reads an out-of-range block, which the copy fills
+  //      with zeros.  Its table entry is read one tile ahead.  The producer
+  //      allocates the tensor memory and issues the tiles whose stages are
+  //      free from the start at once, while the other warps check the rows
+  //      and stage the queries (entries are range-checked below; a copy at
+  //      an out-of-range coordinate only reads fill values).
+  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Cfg::kSlotOff);
+  const uint64_t policy = policy_evict_first();
+  const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
+  auto entry = [&](int j) {
+    const int pos = j * KT + lane * RB;
+    return (fits && lane < Cfg::kBoxes && j < n_tiles && pos < PS)
+               ? make_int2(ld_nc(lrow + pos / BS), pos % BS)
+               : make_int2(oob_block, 0);
+  };
+  auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int2 e, uint32_t bar) {
+    if (lane < Cfg::kBoxes) {
+#pragma unroll
+      for (int h = 0; h < Cfg::kHalves; ++h)
+        tma_load_4d(dst + h * Cfg::kKvHalfBytes + lane * RB * 128, map, h * 64, e.y, kvh, e.x,
+                    bar, policy);
+    }
+  };
+  int jk = 0, jv = 0;  // tiles whose key / value copies were issued
+  int2 cur = make_int2(oob_block, 0);
+  // Tile j's copies once its stages are free; false if a wait gave up.
+  auto issue_tile = [&](int j) {
+    const int2 nxt = entry(j + 1);
+    const int sk = j % NK, sv = j % NV;
+    if (j >= NK &&
+        __any_sync(kFullMask, !mbar_wait(k_empty(sk), (uint32_t)(((j / NK) - 1) & 1))))
+      return false;
+    if (lane == 0) mbar_arrive_expect_tx(k_full(sk), Cfg::kKvBytes);
+    __syncwarp();
+    load_tile(&tmk, sbase + Cfg::kKRingOff + sk * Cfg::kKvBytes, cur, k_full(sk));
+    jk = j + 1;
+    if (j >= NV &&
+        __any_sync(kFullMask, !mbar_wait(v_empty(sv), (uint32_t)(((j / NV) - 1) & 1))))
+      return false;
+    if (lane == 0) mbar_arrive_expect_tx(v_full(sv), Cfg::kKvBytes);
+    __syncwarp();
+    load_tile(&tmv, sbase + Cfg::kVRingOff + sv * Cfg::kKvBytes, cur, v_full(sv));
+    jv = j + 1;
+    cur = nxt;
+    return true;
+  };
+  // Copies issued but possibly never consumed (another role stopped).
+  auto drain_copies = [&]() {
+    for (int j = jk - NK < 0 ? 0 : jk - NK; j < jk; ++j)
+      mbar_wait(k_full(j % NK), (uint32_t)((j / NK) & 1), kWaitLimitNs / 8);
+    for (int j = jv - NV < 0 ? 0 : jv - NV; j < jv; ++j)
+      mbar_wait(v_full(j % NV), (uint32_t)((j / NV) & 1), kWaitLimitNs / 8);
+  };
+  const int npre = fits ? min(n_tiles, min(NK, NV)) : 0;  // no waits before these
+  if (warp == Cfg::kProducerWarp) {
+    tmem_alloc(smem_addr(slot), Cfg::kTmemCols);
+    tmem_relinquish();
+    cur = entry(0);
+    for (int j = 0; j < npre; ++j) issue_tile(j);
+  }
+
   // ---- rows: lane `lane` of softmax warp `warp` (tensor-memory lane
   // 32 warp + lane) is copy `cp` of stacked row R = row0 + r_local.  Loads
   // issued together: its length, its group (shared_owner), its member's
@@ -244,8 +307,23 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
     const int e = ld_nc(lrow + i);
     bad |= (e < 0 || (int64_t)e >= p.num_blocks);
   }
+  // The stacked query rows go to shared memory as soon as they arrive (a row
+  // whose checks fail is computed all the same and its result dropped;
+  // lanes without a row hold zeros).
+  if (warp < 4) {
+    const int qr = warp * 32 + lane;  // this thread's MMA row
+#pragma unroll
+    for (int c = 0; c < D / 8; ++c) {
+      const int h = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + h * Cfg::kQHalfBytes + qr * 128 +
+                                ((cc ^ (qr & 7)) << 4)) = qv[c];
+    }
+    fence_proxy_async_smem();
+  }
   // The leader's entries are unusable: every member's row is marked invalid.
+  tc_fence_before();
   bad = __syncthreads_or(bad);
+  tc_fence_after();
   if (has_row && my_status == 1 &&
       (bad || my_len < tok0 + PS || member_bad[R / G - m_first] != 0))
     my_status = -1;
@@ -285,84 +363,29 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
     for (int c0 = 0; c0 < D; c0 += 32) store_row(true, 0.f, 0.f, zero, c0 + cp * DW);
   };
   if (bad) {  // no tensor-core work: every usable row is now broken
+    if (warp == Cfg::kProducerWarp) {
+      drain_copies();
+      tc_fence_before();
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(*slot, Cfg::kTmemCols);
+    }
     mark_broken_rows(true);
     return;
   }
 
-  // ---- tensor memory; the stacked query rows (zeros where unusable) --------
-  uint32_t* slot = reinterpret_cast<uint32_t*>(smem + Cfg::kSlotOff);
-  if (warp == Cfg::kProducerWarp) {
-    tmem_alloc(smem_addr(slot), Cfg::kTmemCols);
-    tmem_relinquish();
-  }
-  if (warp < 4) {
-    const bool use = has_row && my_status == 1;
-    const int qr = warp * 32 + lane;  // this thread's MMA row
-#pragma unroll
-    for (int c = 0; c < D / 8; ++c) {
-      const int h = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(smem + Cfg::kQOff + h * Cfg::kQHalfBytes + qr * 128 +
-                                ((cc ^ (qr & 7)) << 4)) = use ? qv[c] : make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
   const uint32_t tmem = *slot;
   bool failed = false;
 
   if (warp == Cfg::kProducerWarp) {
-    // ---- producer: key tile j into K stage j % NK, value tile j into V
-    //      stage j % NV.  Lane b < kBoxes copies box b (RB positions); a box
-    //      past the partition's end reads an out-of-range block, which the
-    //      copy fills with zeros.  Its table entry is read one tile ahead.
-    const uint64_t policy = policy_evict_first();
-    const int oob_block = p.num_blocks > 0x7FFFFFFF ? 0x7FFFFFFF : (int)p.num_blocks;
-    auto entry = [&](int j) {
-      const int pos = j * KT + lane * RB;
-      return (lane < Cfg::kBoxes && j < n_tiles && pos < PS)
-                 ? make_int2(ld_nc(lrow + pos / BS), pos % BS)
-                 : make_int2(oob_block, 0);
-    };
-    auto load_tile = [&](const CUtensorMap* map, uint32_t dst, int2 e, uint32_t bar) {
-      if (lane < Cfg::kBoxes) {
-#pragma unroll
-        for (int h = 0; h < Cfg::kHalves; ++h)
-          tma_load_4d(dst + h * Cfg::kKvHalfBytes + lane * RB * 128, map, h * 64, e.y, kvh, e.x,
-                      bar, policy);
-      }
-    };
-    int jk = 0, jv = 0;  // tiles whose key / value copies were issued
-    int2 cur = entry(0);
-    for (int j = 0; j < n_tiles; ++j) {
-      const int2 nxt = entry(j + 1);
-      const int sk = j % NK, sv = j % NV;
-      if (j >= NK &&
-          __any_sync(kFullMask, !mbar_wait(k_empty(sk), (uint32_t)(((j / NK) - 1) & 1)))) {
+    // ---- producer, continued: the remaining tiles as their stages free up
+    for (int j = npre; j < n_tiles; ++j) {
+      if (!issue_tile(j)) {
         failed = true;
         break;
       }
-      if (lane == 0) mbar_arrive_expect_tx(k_full(sk), Cfg::kKvBytes);
-      __syncwarp();
-      load_tile(&tmk, sbase + Cfg::kKRingOff + sk * Cfg::kKvBytes, cur, k_full(sk));
-      jk = j + 1;
-      if (j >= NV &&
-          __any_sync(kFullMask, !mbar_wait(v_empty(sv), (uint32_t)(((j / NV) - 1) & 1)))) {
-        failed = true;
-        break;
-      }
-      if (lane == 0) mbar_arrive_expect_tx(v_full(sv), Cfg::kKvBytes);
-      __syncwarp();
-      load_tile(&tmv, sbase + Cfg::kVRingOff + sv * Cfg::kKvBytes, cur, v_full(sv));
-      jv = j + 1;
-      cur = nxt;
     }
-    // Copies issued but possibly never consumed (another role stopped).
-    for (int j = jk - NK < 0 ? 0 : jk - NK; j < jk; ++j)
-      mbar_wait(k_full(j % NK), (uint32_t)((j / NK) & 1), kWaitLimitNs / 8);
-    for (int j = jv - NV < 0 ? 0 : jv - NV; j < jv; ++j)
-      mbar_wait(v_full(j % NV), (uint32_t)((j / NV) & 1), kWaitLimitNs / 8);
+    drain_copies();
   } else if (warp == Cfg::kMmaWarp) {
     // ---- MMA issuer: S(0); per tile j, S(j+1) once its keys are in and the
     //      softmax has read S(j), then P.V(j) once P(j) and the values are in.
