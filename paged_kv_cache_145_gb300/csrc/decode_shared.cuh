@@ -654,7 +654,7 @@ decode_shared_prefix_kernel(const DecodeParams p, int row_blocks,
 // length or tail table entries are invalid, gets zero rows and its error
 // bit (PKV_DEV_SHARING, PKV_DEV_SEQ_LEN, PKV_DEV_TABLE_RANGE).
 template <typename T, int D, int BS, int G>
-__global__ void __launch_bounds__(128) decode_tail_merge_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(128, (G > 4 ? 4 : 8)) decode_tail_merge_kernel(const DecodeParams p) {
   constexpr int DPL = D / 32;  // dims per lane
   constexpr int NB = 8;        // positions per batch of row loads
   constexpr int NPRE = 2;      // shared partials loaded ahead (the rest in the merge loop)
