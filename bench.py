@@ -52,19 +52,19 @@ from paged_kv_cache_145_gb300 import synth  # noqa: E402
 METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofline"
 
 # DRAM bytes (read + write) per launch of the decode partition kernel (for
-# the shared-prefix decode: of its three kernels together, per call), from
+# the shared-prefix decode: of its kernels together, per call), from
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum), keyed by workload, KV
 # dtype or decode form, and partition length, with the hash of the sources
 # of that kernel family they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b/native/512": (1277835136, "452345e63fe421e3"),
-    "gqa/native/512": (1127102976, "452345e63fe421e3"),
-    "long/native/512": (875536640, "452345e63fe421e3"),
-    "fork/native/512": (77182720, "452345e63fe421e3"),
-    "fork/shared/512": (79988736, "452345e63fe421e3"),
-    "opt13b/fp8/2048": (641391232, "54e1ddb323cddf15"),
-    "gqa/fp8/2048": (563100160, "54e1ddb323cddf15"),
-    "long/fp8/1536": (437307904, "54e1ddb323cddf15"),
+    "opt13b/native/512": (1277795200, "4eefdc81601bea52"),
+    "gqa/native/512": (1127097344, "4eefdc81601bea52"),
+    "long/native/512": (875546240, "4eefdc81601bea52"),
+    "fork/native/512": (77180416, "4eefdc81601bea52"),
+    "fork/shared/512": (77876352, "4eefdc81601bea52"),
+    "opt13b/fp8/2048": (641347072, "4b0ca00c60f77cf6"),
+    "gqa/fp8/2048": (563084544, "4b0ca00c60f77cf6"),
+    "long/fp8/1536": (437377920, "4b0ca00c60f77cf6"),
 }
 
 KERNEL_SOURCES = {

@@ -14,9 +14,10 @@
 // stacked together: with 8 forks and 4 query heads per KV head that is 32
 // query rows against each K/V tile, a dense contraction.  Each member's
 // partial (m, l, o) of such a partition goes to the same workspace slot the
-// plain partition pass would have written, the plain partition pass skips
+// plain partition pass would have written; the plain partition pass skips
 // those partitions, and the split-K merge combines them with the member's
-// own tail unchanged.
+// own tail unchanged (or, when every tail fits in one partition,
+// decode_tail_merge_kernel below computes the tails and merges).
 //
 // Kernel (this library's design), on the fifth-generation tensor cores:
 // grid (KV head, group, shared partition x row block).  The 128 rows of
