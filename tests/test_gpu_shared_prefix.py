@@ -104,16 +104,31 @@ def test_groups_match_oracle(dt, Hk, G, D, b, part):
     plain, err = c.run(part=part, plain=True)
     assert err == 0
     assert np.all(np.abs(got - gpu_out_f64(plain)) <= edge_tol(dt, ref))
+    # Tail grids: as many slices as the longest tail needs (one: the tails
+    # are computed and merged in one pass), and one more.
+    ps = part if part else pkv.paged_attention_partition_size(
+        pkv.PagedKVCache(c.k[:1].cuda(), c.v[:1].cuda()), len(c.lens), Hk * G, c.tables.shape[1] * b)
+    own = {}
+    for gi in range(len(c.starts) - 1):
+        for s_ in range(c.starts[gi], c.starts[gi + 1]):
+            own[s_] = c.prefixes[gi] // ps
+    need = max(-(-L // ps) - own.get(i, 0) for i, L in enumerate(c.lens))
+    for tp in (max(need, 1), need + 1):
+        out, err = c.run(part=part, tail_parts=tp)
+        assert err == 0, (tp, need)
+        assert np.all(np.abs(gpu_out_f64(out) - ref) <= edge_tol(dt, ref)), tp
 
 
 def test_group_larger_than_one_row_block():
     # 12 members x 8 query heads = 96 stacked rows: three row blocks.
     groups = [(12, 256, [256 + 3 * i for i in range(12)]), (1, 0, [33])]
     c = GroupCase("bf16", 1, 8, 128, 16, groups, seed=5)
-    out, err = c.run(part=64)
-    assert err == 0
-    got, ref = gpu_out_f64(out), c.oracle()
-    assert np.all(np.abs(got - ref) <= edge_tol("bf16", ref))
+    ref = c.oracle()
+    for tp in (0, 1):  # every tail (<= 33 positions) within one 64-position partition
+        out, err = c.run(part=64, tail_parts=tp)
+        assert err == 0
+        got = gpu_out_f64(out)
+        assert np.all(np.abs(got - ref) <= edge_tol("bf16", ref))
 
 
 def test_parallel_sampling_workload_full_size_all_sequences():
