@@ -835,7 +835,7 @@ prefill_tc_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap tmk
         // P: keys 2c, 2c+1 in column c (high part, or the only one); a low
         // part of the same keys in column 32 + c.  fp16 unless this is a bf16
         // tile whose values need the bf16 two-part path (the converters'
-        // verdict on tile j, published before they arrive on vt_full).
+        // decision on tile j, published before they arrive on vt_full).
         bool wide = false;
         if constexpr (Cfg::kWideCheck) {
           const bool got = mbar_wait(vt_full(j % NV), (uint32_t)((j / NV) & 1));
