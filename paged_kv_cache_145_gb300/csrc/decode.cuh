@@ -127,10 +127,26 @@ __device__ __forceinline__ int shared_owner(const DecodeParams& p, int s) {
   return (a <= s && s < b) ? lo + g : -1;
 }
 
+// shared_owner for a sequence s that every lane of the warp asks about: the
+// same function, with the last round's probes spread over the lanes (one
+// load each, a ballot) when the list has at most 32 groups.
+__device__ __forceinline__ int shared_owner_warp(const DecodeParams& p, int s) {
+  if (!p.group_starts || p.num_groups <= 0) return -1;
+  if (p.num_groups > 32) return shared_owner(p, s);
+  const int lane = threadIdx.x & 31, n = p.num_groups;
+  const int v = lane <= n ? ld_nc(p.group_starts + lane) : 0;  // entries 0 .. n (n <= 32)
+  const int v32 = n == 32 ? ld_nc(p.group_starts + 32) : 0;
+  const unsigned hit = __ballot_sync(kFullMask, lane >= 1 && lane < n && v <= s);
+  const int g = hit ? 31 - __clz(hit) : 0;  // the last candidate with its start <= s
+  const int a = __shfl_sync(kFullMask, v, g);
+  const int b = g + 1 == 32 ? v32 : __shfl_sync(kFullMask, v, (g + 1) & 31);
+  return (a <= s && s < b) ? g : -1;
+}
+
 // Partitions of sequence s that the shared-prefix kernel computes (at most
-// the grid's partitions).
+// the grid's partitions); s is the same for every lane of the warp.
 __device__ __forceinline__ int shared_parts_of(const DecodeParams& p, int s) {
-  const int g = shared_owner(p, s);
+  const int g = shared_owner_warp(p, s);
   if (g < 0) return 0;
   const int pre = ld_nc(p.group_prefix + g);
   return pre > 0 ? min(pre / p.part_size, p.num_parts) : 0;

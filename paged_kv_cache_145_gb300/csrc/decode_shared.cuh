@@ -680,7 +680,11 @@ __global__ void __launch_bounds__(128, (G > 4 ? 4 : 8)) decode_tail_merge_kernel
       RowLoad<T, DPL>::load(static_cast<const T*>(p.q) + ((int64_t)s * H + kvh * G + g) * D +
                                 lane * DPL, q[hh]);
   }
-  const int first = shared_parts_of(p, s);  // partitions the shared-prefix kernel computed
+  // Partitions the shared-prefix kernel computed (shared_parts_of, with the
+  // group lookup spread over each warp's lanes).
+  const int g_own = shared_owner_warp(p, s);
+  const int pre = g_own >= 0 ? ld_nc(p.group_prefix + g_own) : 0;
+  const int first = pre > 0 ? min(pre / PS, p.num_parts) : 0;
   auto zero_rows = [&]() {
     for (int e = threadIdx.x; e < G * D; e += 128) out[out0 + e] = Elem<T>::from_f(0.f);
   };
