@@ -57,14 +57,14 @@ METRIC = "paged decode attention KV GB/s and tokens/s on 1 GB300, % of HBM roofl
 # dtype or decode form, and partition length, with the hash of the sources
 # of that kernel family they were taken on.  A stale hash reports null.
 TRAFFIC = {
-    "opt13b/native/512": (1277795200, "4eefdc81601bea52"),
-    "gqa/native/512": (1127097344, "4eefdc81601bea52"),
-    "long/native/512": (875546240, "4eefdc81601bea52"),
-    "fork/native/512": (77180416, "4eefdc81601bea52"),
-    "fork/shared/512": (77876352, "4eefdc81601bea52"),
-    "opt13b/fp8/2048": (641347072, "4b0ca00c60f77cf6"),
-    "gqa/fp8/2048": (563084544, "4b0ca00c60f77cf6"),
-    "long/fp8/1536": (437377920, "4b0ca00c60f77cf6"),
+    "opt13b/native/512": (1277931520, "c5e6dfe8a34e9dc5"),
+    "gqa/native/512": (1127068928, "c5e6dfe8a34e9dc5"),
+    "long/native/512": (875515520, "c5e6dfe8a34e9dc5"),
+    "fork/native/512": (77181440, "c5e6dfe8a34e9dc5"),
+    "fork/shared/512": (79970304, "c5e6dfe8a34e9dc5"),
+    "opt13b/fp8/2048": (641383936, "13cf79d9ff22aa7b"),
+    "gqa/fp8/2048": (563038336, "13cf79d9ff22aa7b"),
+    "long/fp8/1536": (437340288, "13cf79d9ff22aa7b"),
 }
 
 KERNEL_SOURCES = {
