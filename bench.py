@@ -842,16 +842,10 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
     has_pairs = len(w.pairs) > 0
     nparts_max = -(-w.max_len // part)
     shared = name == "fork" and args.decode == "shared"
-    decode_launches = 1 + (1 if nparts_max > 1 else 0) + (1 if shared else 0)
-    launches_per_step = 1 + decode_launches + (1 if has_pairs else 0)
-
-    stream = torch.cuda.current_stream()
-
-    resident = (q, k, v, slots, tables, lens, pairs)
-
     # Forked batches (the parallel-sampling workload) decode their shared
     # prompt once per group with the shared-prefix entry point; --decode
     # plain times the plain decode instead.
+    tail_parts = 0
     if shared:
         groups, forks = w.cfg["groups"], w.cfg["forks"]
         g_starts = torch.arange(0, groups * forks + 1, forks, dtype=torch.int32, device=dev)
@@ -861,6 +855,20 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
         # shared ones: the host knows every length and prefix.
         tail_parts = max(-(-int(L) // part) for L in w.seq_lens) - \
             ((w.cfg["prompt"] // w.b) * w.b) // part
+    # Kernels per decode call: partition pass (+ merge when any sequence has
+    # several partitions); shared-prefix decode: its kernel, then either the
+    # tail-and-merge pass (every tail within one partition) or the partition
+    # pass and merge.
+    if shared and 0 < tail_parts < nparts_max and tail_parts == 1:
+        decode_launches = 2
+    else:
+        decode_launches = 1 + (1 if nparts_max > 1 else 0) + (1 if shared else 0)
+    launches_per_step = 1 + decode_launches + (1 if has_pairs else 0)
+
+    stream = torch.cuda.current_stream()
+
+    resident = (q, k, v, slots, tables, lens, pairs)
+
 
     def decode(x=resident, o=out):
         if shared:
@@ -1039,8 +1047,10 @@ def decode_line(args, name, cpu, rank, local_rank, world, dev):
                     "(no projections, MLP or sampling)" % layers},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("paged_attention_decode_shared (shared-prefix pass + partition "
-                                "pass + split-K merge)" if shared else
+                     "kernel": (("paged_attention_decode_shared (shared-prefix pass + tail and "
+                                 "merge)" if decode_launches == 2 else
+                                 "paged_attention_decode_shared (shared-prefix pass + partition "
+                                 "pass + split-K merge)") if shared else
                                 "paged_attention_decode (partition pass + split-K merge)"),
                      "peak_source": peak_kind,
                      "peak_note": ("the measured device-to-device copy rate (half reads, half "
